@@ -1,0 +1,194 @@
+"""GB300-native block-quantized weight-only matmul (NVFP4 / FP8 weights).
+
+Thin Python binding over the C-ABI library ``libwqmm.so`` (see
+``include/wqmm.h``).  This module only marshals arguments: every step of the
+computation runs in the library's CUDA kernels.  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the library is
+missing or fails to load, importing the entry points raises.
+
+Raw C-ABI access (same names and arguments as the header): ``lib()``.
+Torch-tensor wrappers (same names):
+
+* ``fp4_weight_matmul(A, B_packed, weight_scale, weight_scale_2, bias=None,
+  block_size=16, out=None)`` -- N = B_packed.shape[0], K = 2 * B_packed.shape[1],
+  M = prod(A.shape[:-1]), Y has A's leading dims and last dim N
+  ("MatMulBlockQuantizedFp4Weight - CUDA Operator Documentation" §1).
+* ``fp8_weight_matmul(A, B, b_scale, bias=None, block_size=128, out=None)``
+  ("MatMulBlockQuantizedFp8Weight - CUDA Operator Documentation" §1).
+* ``fp4_dequantize(B_packed, weight_scale, weight_scale_2, block_size=16,
+  dtype=torch.bfloat16, out=None)`` and ``fp8_dequantize(...)``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "WqmmError", "lib", "library_path", "fp4_weight_matmul", "fp8_weight_matmul",
+    "fp4_dequantize", "fp8_dequantize", "device_status", "FP16", "BF16",
+]
+
+FP16 = 0
+BF16 = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libwqmm.so")
+_lib = None
+_lock = threading.Lock()
+
+STATUS = {
+    0: "WQMM_OK", 1: "WQMM_ERR_INVALID_ARG", 2: "WQMM_ERR_UNSUPPORTED",
+    3: "WQMM_ERR_MISALIGNED", 4: "WQMM_ERR_CUDA", 5: "WQMM_ERR_TIMEOUT",
+}
+
+# Exported C symbols, in header order.
+SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp4_dequantize", "fp8_dequantize",
+           "wqmm_status_string", "wqmm_device_status", "wqmm_version")
+
+
+class WqmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded C library with argtypes set (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(or python -m fp8_weight_only_nvfp4_gb300._build)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.fp4_weight_matmul.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P]
+        L.fp8_weight_matmul.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
+        L.fp4_dequantize.argtypes = [P, P, P, P, I64, I64, I, I, P]
+        L.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, I, P]
+        L.wqmm_status_string.argtypes = [I]
+        L.wqmm_status_string.restype = ctypes.c_char_p
+        L.wqmm_device_status.argtypes = [P]
+        L.wqmm_version.argtypes = []
+        for name in ("fp4_weight_matmul", "fp8_weight_matmul", "fp4_dequantize",
+                     "fp8_dequantize", "wqmm_device_status", "wqmm_version"):
+            getattr(L, name).restype = I
+        _lib = L
+        return L
+
+
+# ---------------------------------------------------------------------------
+# torch wrappers (argument marshalling only)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dt(dtype) -> int:
+    torch = _torch()
+    if dtype == torch.bfloat16:
+        return BF16
+    if dtype == torch.float16:
+        return FP16
+    raise TypeError(f"activation dtype must be float16 or bfloat16, got {dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise WqmmError(status, where)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("all tensors must be CUDA tensors (no CPU fallback)")
+            if not t.is_contiguous():
+                raise ValueError("all tensors must be contiguous")
+
+
+def fp4_weight_matmul(A, B_packed, weight_scale, weight_scale_2, bias=None, block_size=16,
+                      out=None, stream=None):
+    torch = _torch()
+    _need_cuda(A, B_packed, weight_scale, weight_scale_2, bias, out)
+    N = B_packed.shape[0]
+    K = 2 * B_packed.shape[1]
+    if A.shape[-1] != K:
+        raise ValueError(f"A.shape[-1]={A.shape[-1]} != K={K}")
+    M = A.numel() // K if K else int(torch.tensor(A.shape[:-1]).prod())
+    if out is None:
+        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=A.device)
+    st = lib().fp4_weight_matmul(_ptr(A), _ptr(B_packed), _ptr(weight_scale),
+                                 _ptr(weight_scale_2), _ptr(bias), _ptr(out), M, N, K,
+                                 int(block_size), _dt(A.dtype), _stream(stream))
+    _check(st, "fp4_weight_matmul")
+    return out
+
+
+def fp8_weight_matmul(A, B, b_scale, bias=None, block_size=128, out=None, stream=None):
+    torch = _torch()
+    _need_cuda(A, B, b_scale, bias, out)
+    N, K = B.shape
+    if A.shape[-1] != K:
+        raise ValueError(f"A.shape[-1]={A.shape[-1]} != K={K}")
+    M = A.numel() // K if K else int(torch.tensor(A.shape[:-1]).prod())
+    if out is None:
+        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=A.device)
+    st = lib().fp8_weight_matmul(_ptr(A), _ptr(B), _ptr(b_scale), _ptr(bias), _ptr(out), M, N,
+                                 K, int(block_size), _dt(A.dtype), _stream(stream))
+    _check(st, "fp8_weight_matmul")
+    return out
+
+
+def fp4_dequantize(B_packed, weight_scale, weight_scale_2, block_size=16, dtype=None,
+                   out=None, stream=None):
+    torch = _torch()
+    _need_cuda(B_packed, weight_scale, weight_scale_2, out)
+    dtype = torch.bfloat16 if dtype is None else dtype
+    N = B_packed.shape[0]
+    K = 2 * B_packed.shape[1]
+    if out is None:
+        out = torch.empty(N, K, dtype=dtype, device=B_packed.device)
+    st = lib().fp4_dequantize(_ptr(B_packed), _ptr(weight_scale), _ptr(weight_scale_2),
+                              _ptr(out), N, K, int(block_size), _dt(out.dtype), _stream(stream))
+    _check(st, "fp4_dequantize")
+    return out
+
+
+def fp8_dequantize(B, b_scale, block_size=128, dtype=None, out=None, stream=None):
+    torch = _torch()
+    _need_cuda(B, b_scale, out)
+    dtype = torch.bfloat16 if dtype is None else dtype
+    N, K = B.shape
+    if out is None:
+        out = torch.empty(N, K, dtype=dtype, device=B.device)
+    st = lib().fp8_dequantize(_ptr(B), _ptr(b_scale), _ptr(out), N, K, int(block_size),
+                              _dt(out.dtype), _stream(stream))
+    _check(st, "fp8_dequantize")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    return int(lib().wqmm_device_status(_stream(stream)))

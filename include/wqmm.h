@@ -1,0 +1,146 @@
+/*
+ * wqmm.h -- block-quantized weight-only matrix multiplication for NVIDIA
+ * GB300 (sm_103a): NVFP4 and FP8 (E4M3) weights, FP16/BF16 activations.
+ *
+ *     Y[M, N] = A[M, K] * dequant(B)[N, K]^T (+ bias[N])
+ *
+ * Sources (web pages, by title and section):
+ *   [FP4]  "MatMulBlockQuantizedFp4Weight - CUDA Operator Documentation"
+ *   [FP8]  "MatMulBlockQuantizedFp8Weight - CUDA Operator Documentation"
+ *   [BLOG] "ONNX Runtime #32128 -- Why Dequantizing 4-Bit Weights Became the
+ *          Most Expensive Kernel in H200 Prefill"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer (global memory of the current
+ *    device), row-major and contiguous.  The caller owns every buffer.  The
+ *    library allocates no device memory and keeps no per-call state.
+ *  - `dtype` selects the activation type used for A, bias, Y and dequantized
+ *    outputs: WQMM_FP16 (IEEE binary16) or WQMM_BF16 (bfloat16).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is asynchronous on that stream; the return value
+ *    reports argument checks and launch errors only.
+ *  - Base pointers must be 16-byte aligned (WQMM_ERR_MISALIGNED otherwise).
+ *  - Empty outputs (M == 0 or N == 0) return WQMM_OK without launching
+ *    ([FP4] §3 and [FP8] §3: the dispatch chain returns on empty output).
+ *  - K == 0 with a non-empty output writes Y = bias (or zeros).
+ *  - No entry point traps or aborts.  Waits inside the kernels are bounded;
+ *    a wait that runs out records WQMM_ERR_TIMEOUT in a device word that
+ *    wqmm_device_status() reports.
+ *  - Thread safety: calls may be issued from several host threads at once.
+ *    Per-device setup (kernel attributes, driver entry points) runs once.
+ */
+#ifndef WQMM_H_
+#define WQMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WQMM_FP16 = 0,
+  WQMM_BF16 = 1
+} wqmm_dtype;
+
+typedef enum {
+  WQMM_OK = 0,
+  WQMM_ERR_INVALID_ARG = 1,  /* null pointer, negative size, odd K (FP4), block_size < 1 */
+  WQMM_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+  WQMM_ERR_MISALIGNED = 3,   /* a base pointer is not 16-byte aligned */
+  WQMM_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  WQMM_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out */
+} wqmm_status;
+
+/*
+ * fp4_weight_matmul -- Y = A * dequant(B)^T (+ bias) with an NVFP4 weight.
+ * [FP4] §1 Operator Schema, §2 Weight Format:
+ *     B_dequant[n, k] = e2m1(B[n, k]) * e4m3(weight_scale[n, k / block_size])
+ *                       * weight_scale_2
+ *
+ *   A              [M, K] activations (dtype).
+ *   B_packed       [N, K/2] uint8: two E2M1 codes per byte, the LOW nibble
+ *                  holds the even k, the HIGH nibble the odd k.
+ *   weight_scale   [N, S] uint8 raw E4M3FN bytes, S = ceil(K / block_size);
+ *                  element k uses column floor(k / block_size).
+ *   weight_scale_2 one float32 global scale, read on the device.
+ *   bias           [N] (dtype) or NULL.
+ *   Y              [M, N] output (dtype), written with one round-to-nearest-
+ *                  even from the float32 value  acc * weight_scale_2 + bias.
+ *   M, N, K        sizes; M is the product of A's leading dimensions.
+ *   block_size     K elements per scale; must be a positive multiple of 16.
+ *
+ * Paths: M <= 8 runs the decode GEMV (each weight byte read once, the decode
+ * shared by all M rows); larger M with K % 32 == 0 runs the fused tcgen05
+ * GEMM (the weight is dequantized inside the main loop, no [N, K] scratch);
+ * other shapes run the GEMV once per 8-row group of A.
+ * Errors: odd K or block_size < 1 -> INVALID_ARG; block_size % 16 != 0 ->
+ * UNSUPPORTED; any size < 0 -> INVALID_ARG.
+ * Accuracy: |Y - Y_exact| <= 8e-3 * sum_k |A * B_dq| + 1e-3 (BF16) and
+ * <= 2e-3 * sum_k |A * B_dq| + 1e-4 (FP16), Y_exact in exact arithmetic.
+ */
+int fp4_weight_matmul(const void* A, const uint8_t* B_packed,
+                      const uint8_t* weight_scale, const float* weight_scale_2,
+                      const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
+                      int block_size, int dtype, void* stream);
+
+/*
+ * fp8_weight_matmul -- Y = A * dequant(B)^T (+ bias) with an FP8 E4M3 weight.
+ * [FP8] §2 Tensor and Scale Format:
+ *     B_dequant[n, k] = fp8_e4m3(B[n, k]) * b_scale[n, k / block_size]
+ *
+ *   A        [M, K] activations (dtype).
+ *   B        [N, K] uint8 E4M3FN bytes.
+ *   b_scale  [N, S] float32, S = ceil(K / block_size); a partial final block
+ *            uses the last column.
+ *   bias     [N] (dtype) or NULL.
+ *   Y        [M, N] (dtype).
+ *   block_size must be a positive multiple of 16.
+ * Paths as for fp4_weight_matmul (the GEMM needs K % 16 == 0).
+ * Accuracy bound as for fp4_weight_matmul.
+ */
+int fp8_weight_matmul(const void* A, const uint8_t* B, const float* b_scale,
+                      const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
+                      int block_size, int dtype, void* stream);
+
+/*
+ * fp4_dequantize -- expand an NVFP4 weight to the activation type.
+ * [FP4] §2 formula, §5 step 1; [BLOG] vectorised dequant.
+ *   out[n, k] = RNE_dtype( fp32( fp32(e2m1 * e4m3) * weight_scale_2 ) )
+ * The first product is exact in fp32; the multiply by weight_scale_2 rounds
+ * once (fp32, nearest even); the conversion to dtype rounds once more.  The
+ * result is bit-exact to that definition.
+ *   out  [N, K] (dtype).  Any block_size >= 1 (odd included) and any even K.
+ */
+int fp4_dequantize(const uint8_t* B_packed, const uint8_t* weight_scale,
+                   const float* weight_scale_2, void* out, int64_t N, int64_t K,
+                   int block_size, int dtype, void* stream);
+
+/*
+ * fp8_dequantize -- expand an FP8 weight to the activation type.
+ * [FP8] §2 formula, §5 step 1.
+ *   out[n, k] = RNE_dtype( fp32(e4m3(B[n, k]) * b_scale[n, k / block_size]) )
+ * Bit-exact to that definition.  Any K >= 0 and block_size >= 1.
+ */
+int fp8_dequantize(const uint8_t* B, const float* b_scale, void* out,
+                   int64_t N, int64_t K, int block_size, int dtype, void* stream);
+
+/* Human-readable name of a wqmm_status value (static string). */
+const char* wqmm_status_string(int status);
+
+/*
+ * wqmm_device_status -- synchronise `stream`, then return and clear the
+ * device-side error word (WQMM_OK if no bounded wait ran out since the last
+ * call), or WQMM_ERR_CUDA if the synchronisation itself failed.
+ */
+int wqmm_device_status(void* stream);
+
+/* Version of this interface (major * 100 + minor). */
+int wqmm_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* WQMM_H_ */

@@ -1,0 +1,111 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/wqmm.h declares, and rejects bad arguments on the host (no compute
+call is made here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_weight_only_nvfp4_gb300 as wq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "wqmm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return [n for n in names if n not in ("if", "while")]
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_weight_only_nvfp4_gb300 import _build
+    _build.build()
+    return wq.lib()
+
+
+def test_header_declares_the_expected_api():
+    names = _header_functions()
+    assert set(names) == set(wq.SYMBOLS), names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _header_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    for code, name in wq.STATUS.items():
+        assert L.wqmm_status_string(code).decode() == name
+    assert L.wqmm_status_string(99).decode() == "WQMM_ERR_UNKNOWN"
+    assert L.wqmm_version() == 100
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)        # 16-byte aligned non-null address (never dereferenced)
+FAKE_ODD = P(0x10001)
+
+
+def fp4mm(L, M=4, N=16, K=32, bs=16, dt=1, A=FAKE, B=FAKE, ws=FAKE, ws2=FAKE, bias=None, Y=FAKE):
+    return L.fp4_weight_matmul(A, B, ws, ws2, bias, Y, M, N, K, bs, dt, None)
+
+
+def test_fp4_matmul_argument_checks(L):
+    assert fp4mm(L, dt=2) == 1
+    assert fp4mm(L, M=-1) == 1
+    assert fp4mm(L, K=31) == 1          # odd K cannot be packed two per byte
+    assert fp4mm(L, bs=0) == 1
+    assert fp4mm(L, bs=8) == 2          # block size must be a multiple of 16
+    assert fp4mm(L, bs=24) == 2
+    assert fp4mm(L, A=None) == 1
+    assert fp4mm(L, B=None) == 1
+    assert fp4mm(L, ws=None) == 1
+    assert fp4mm(L, ws2=None) == 1
+    assert fp4mm(L, Y=None) == 1
+    assert fp4mm(L, A=FAKE_ODD) == 3
+    assert fp4mm(L, Y=FAKE_ODD) == 3
+    assert fp4mm(L, B=FAKE_ODD) == 3
+    assert fp4mm(L, bias=FAKE_ODD) == 3  # 2-byte alignment for bias
+    # empty outputs return OK without touching the GPU
+    assert fp4mm(L, M=0, A=None, Y=None) == 0
+    assert fp4mm(L, N=0, A=None, Y=None) == 0
+
+
+def test_fp8_matmul_argument_checks(L):
+    f = lambda **kw: L.fp8_weight_matmul(kw.get("A", FAKE), kw.get("B", FAKE),
+                                         kw.get("s", FAKE), None, kw.get("Y", FAKE),
+                                         kw.get("M", 4), kw.get("N", 16), kw.get("K", 32),
+                                         kw.get("bs", 128), kw.get("dt", 1), None)
+    assert f(dt=-1) == 1
+    assert f(K=-5) == 1
+    assert f(bs=-1) == 1
+    assert f(bs=100) == 2
+    assert f(s=None) == 1
+    assert f(s=FAKE_ODD) == 3
+    assert f(M=0, A=None, Y=None) == 0
+
+
+def test_dequant_argument_checks(L):
+    assert L.fp4_dequantize(FAKE, FAKE, FAKE, FAKE, 4, 33, 16, 1, None) == 1   # odd K
+    assert L.fp4_dequantize(FAKE, FAKE, FAKE, FAKE, 4, 32, 0, 1, None) == 1    # bs < 1
+    assert L.fp4_dequantize(FAKE, FAKE, FAKE, None, 4, 32, 16, 1, None) == 1
+    assert L.fp4_dequantize(FAKE, FAKE_ODD, FAKE, FAKE, 4, 32, 16, 1, None) == 3
+    assert L.fp4_dequantize(None, None, None, None, 0, 32, 16, 1, None) == 0    # empty
+    assert L.fp4_dequantize(None, None, None, None, 5, 0, 16, 1, None) == 0
+    assert L.fp8_dequantize(FAKE, FAKE, FAKE, 4, 32, 16, 3, None) == 1
+    assert L.fp8_dequantize(FAKE, None, FAKE, 4, 32, 16, 1, None) == 1
+    assert L.fp8_dequantize(FAKE_ODD, FAKE, FAKE, 4, 32, 16, 1, None) == 3
+
+
+def test_torch_wrappers_refuse_cpu_tensors(L):
+    import torch
+    A = torch.zeros(1, 32, dtype=torch.bfloat16)
+    B = torch.zeros(16, 16, dtype=torch.uint8)
+    ws = torch.zeros(16, 2, dtype=torch.uint8)
+    ws2 = torch.ones(1)
+    with pytest.raises(ValueError):
+        wq.fp4_weight_matmul(A, B, ws, ws2)

@@ -27,8 +27,14 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-// Iteration limit for every spin-wait (about a second or more at GPU clocks).
-constexpr uint32_t kSpinLimit = 1u << 26;
+// Every spin-wait in this library gives up after this much wall time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // ---------------------------------------------------------------------------
 // Address helpers
@@ -74,8 +80,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // false (and records WQMM_ERR_TIMEOUT in *err) if the limit runs out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
+    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
   record_error(err, 5 /* WQMM_ERR_TIMEOUT */);
   return false;

@@ -31,6 +31,8 @@ def bits_of(t):
 
 
 def f64_of(t):
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
     return t.float().cpu().numpy().astype(np.float64)
 
 

@@ -1,0 +1,99 @@
+"""Fused dequantize + tcgen05 GEMM (M > 8) parity against the oracle."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from gpu_util import act_to_dev, assert_within_tolerance, f64_of, fp4_dev, run_fp4, run_fp8
+
+pytestmark = pytest.mark.gpu
+
+
+def _ref(p):
+    return oracle.fp4_matmul(p.A, p.B_packed, p.weight_scale, p.weight_scale_2, p.bias, p.M, p.N,
+                             p.K, p.block_size, p.dtype)
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+@pytest.mark.parametrize("M,N,K,bs", [
+    (16, 128, 64, 16), (256, 128, 128, 16), (9, 1, 32, 16), (300, 200, 320, 16),
+    (17, 129, 96, 32), (257, 255, 1024, 16), (512, 384, 2048, 64), (100, 64, 5120, 16),
+])
+def test_small_shapes(M, N, K, bs, dtype):
+    p = wl.make_fp4(M, N, K, bs, dtype, seed=M * 3 + N + K, bias_sigma=0.05)
+    assert_within_tolerance(run_fp4(p), *_ref(p), dtype, f"gemm {M}x{N}x{K} bs={bs}")
+
+
+def test_one_hot_probe_gemm():
+    """Bit-exact one-hot probe through the GEMM path (weight_scale_2 = 1, no
+    bias): token m selects column k(m) of the weight; Y[m, n] = B_dq[n, k(m)]."""
+    M, N, K, bs = 256, 128, 256, 16
+    p = wl.make_fp4(M, N, K, bs, oracle.BF16, seed=17, ws2=1.0)
+    d = fp4_dev(p)
+    W = oracle.fp4_dequantize_f64(p.B_packed, p.weight_scale, 1.0, N, K, bs)
+    for shift in (0, 1, 101):
+        ks = (np.arange(M) * 7 + shift) % K
+        A = np.zeros((M, K))
+        A[np.arange(M), ks] = 1.0
+        d["A"] = act_to_dev(wl.act_bits(A, p.dtype), p.dtype)
+        Y = f64_of(run_fp4(p, d))
+        assert np.array_equal(Y, W[:, ks].T), shift
+
+
+def _sampled_check(p, run, ref_sampled, seed=0, n_random=4096, full_rows=4, full_cols=4):
+    Y = f64_of(run(p)).reshape(p.M, p.N)
+    r = np.random.Generator(np.random.PCG64(seed))
+    ms = [r.integers(0, p.M, n_random)]
+    ns = [r.integers(0, p.N, n_random)]
+    for m in r.integers(0, p.M, full_rows):
+        ms.append(np.full(p.N, m))
+        ns.append(np.arange(p.N))
+    for n in r.integers(0, p.N, full_cols):
+        ms.append(np.arange(p.M))
+        ns.append(np.full(p.M, n))
+    ms = np.concatenate(ms).astype(np.int64)
+    ns = np.concatenate(ns).astype(np.int64)
+    Yr, S = ref_sampled(p, ms, ns)
+    return assert_within_tolerance(Y[ms, ns], Yr, S, p.dtype, "sampled")
+
+
+def _fp4_sampled(p, ms, ns):
+    return oracle.fp4_matmul_sampled(p.A, p.B_packed, p.weight_scale, p.weight_scale_2, p.bias,
+                                     p.K, p.block_size, p.dtype, ms, ns)
+
+
+@pytest.mark.parametrize("shape", ["gate_up", "down"])
+def test_prefill_full_size_sampled(shape):
+    """NVFP4 prefill M=8192: gate/up (N=17408, K=5120) and down (N=5120,
+    K=17408), in the launch configuration the benchmark times; outputs checked
+    at 4096 random positions plus 4 full rows and 4 full columns."""
+    p = wl.prefill(shape)
+    _sampled_check(p, run_fp4, _fp4_sampled)
+
+
+def test_fp8_gemm_shapes():
+    for (M, N, K, bs) in [(64, 128, 256, 128), (300, 257, 1024, 64), (16, 96, 5120, 128)]:
+        p = wl.make_fp8(M, N, K, bs, oracle.BF16, seed=K, bias_sigma=0.02)
+        Yr, S = oracle.fp8_matmul(p.A, p.B, p.b_scale, p.bias, M, N, K, bs, p.dtype)
+        assert_within_tolerance(run_fp8(p), Yr, S, p.dtype, f"fp8 gemm {M}x{N}x{K}")
+
+
+def test_fp8_prefill_sampled():
+    """FP8 M=8192, N=17408, K=5120, bs=128."""
+    p = wl.fp8_problem(8192, N=17408, K=5120, bias_sigma=0.02)
+
+    def ref(p, ms, ns):
+        return oracle.fp8_matmul_sampled(p.A, p.B, p.b_scale, p.bias, p.K, p.block_size,
+                                         p.dtype, ms, ns)
+    _sampled_check(p, run_fp8, ref)
+
+
+def test_fp8_tail_prefill_sampled():
+    """FP8 K=5000 (partial last block) at M=8192 takes the row-group GEMV path."""
+    p = wl.fp8_problem(8192, N=5120, K=5000, bias_sigma=0.02)
+
+    def ref(p, ms, ns):
+        return oracle.fp8_matmul_sampled(p.A, p.B, p.b_scale, p.bias, p.K, p.block_size,
+                                         p.dtype, ms, ns)
+    _sampled_check(p, run_fp8, ref, n_random=2048, full_rows=2, full_cols=2)

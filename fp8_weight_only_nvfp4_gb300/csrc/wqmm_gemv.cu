@@ -27,6 +27,9 @@
 //
 // Per-row results do not depend on M: a row's products and their summation
 // order are fixed by (n, k) alone.
+#include <algorithm>
+#include <mutex>
+
 #include "wqmm_device.cuh"
 
 namespace wqmm {
@@ -287,9 +290,394 @@ int launch_general_t(const GemvArgs& a, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 
+
+// ===========================================================================
+// Fast decode GEMV (the path for M <= 8 with K % 32 == 0, block_size a power
+// of two >= 16, NVFP4 or FP8 weight).
+//
+// * CTA = 8 warps = 128 weight rows (warp w owns rows 16w .. 16w + 15), all M
+//   activation rows.  A thread-block cluster of C CTAs along gridDim.y splits
+//   K: rank r takes 128-k windows [r * wpc, (r + 1) * wpc).  Partial sums go
+//   to rank 0 through distributed shared memory and are added there in rank
+//   order (deterministic; no global scratch).
+// * Every lane issues the weight loads of a whole chunk of WPC windows before
+//   decoding anything (16 B per row per window, two rows per lane), and the
+//   next chunk's loads are in flight while the current one is decoded: with
+//   two CTAs per SM that is 64 KB of weight in flight per SM.
+// * The CTA's K-range of the activation is staged once in shared memory (row
+//   pitch an odd multiple of 16 bytes, so the fragment reads of the active
+//   lanes hit distinct banks).
+// * mma.m16n8k16 (FP16 or BF16 operands, FP32 accumulate), weight as the A
+//   operand.  Lane (g, t) owns k in [w*128 + 32t, w*128 + 32t + 32) of rows
+//   g, g + 8 and activation row g; MMA j of a window takes k = 32t + 4j .. +1
+//   into k-slots 2t, 2t + 1 and k = 32t + 4j + 2 .. +3 into 2t + 8, 2t + 9.
+// * Decode per packed byte: cvt.rn.f16x2.e2m1x2, then for FP16 activations one
+//   f16x2 multiply by the block scale (exact), for BF16 two mixed
+//   f16 x f16 -> f32 multiplies (exact) and one pack to bf16x2 (exact).
+// * Programmatic dependent launch: before griddepcontrol.wait the kernel only
+//   prefetches its weight rows into L2 (never stale: L2 is the point of
+//   coherence), so it may overlap the previous kernel's tail.
+// ===========================================================================
+
+constexpr int kFastWarps = 8;
+constexpr int kFastRows = kFastWarps * 16;
+// 128-k windows per register chunk: 4 for NVFP4 (16 B per row per window),
+// 2 for FP8 (32 B per row per window): 128 B of weight per lane either way.
+template <int KIND>
+constexpr int wpc_of() { return KIND == 0 ? 4 : 2; }
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1, int dt) {
+  if (dt == 1)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One packed NVFP4 byte (in the low 8 bits of `byte`) times an f16 scale ->
+// a 16-bit operand pair (low nibble in the low half).  Exact.
+template <int DT>
+__device__ __forceinline__ uint32_t fp4_pair(uint32_t byte, uint32_t sc16x2) {
+  uint32_t h;
+  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(h) : "r"(byte));
+  if constexpr (DT == 0) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));
+    return r;
+  } else {
+    float lo, hi;
+    fold_pair_f16(h, sc16x2 & 0xFFFFu, lo, hi);
+    return pack2_rn<1>(lo, hi);
+  }
+}
+
+// FP8: two E4M3 bytes (low 16 bits) times a float scale -> operand pair,
+// rounded once to the activation type.
+template <int DT>
+__device__ __forceinline__ uint32_t fp8_pair(uint32_t two, float sc) {
+  const float2 e = f16x2_to_f32x2(e4m3x2_to_f16x2(two));
+  return pack2_rn<DT>(e.x * sc, e.y * sc);
+}
+
+struct FastParams {
+  const uint16_t* A;
+  const uint8_t* B;
+  const uint8_t* ws;      // NVFP4 scales
+  const float* gscale;
+  const float* fscale;    // FP8 scales
+  const uint16_t* bias;
+  uint16_t* Y;
+  int M, N, K;
+  int bs_shift;           // log2(block_size)
+  int wpc;                // 128-k windows per cluster rank
+  int act_pitch;          // activation smem row pitch, bytes
+  int* err;
+};
+
+template <int DT, int KIND>
+struct Chunk {
+  // NVFP4: 16 B per row per window; FP8: 32 B per row per window.
+  static constexpr int kV = (KIND == 0) ? 1 : 2;
+  static constexpr int kWpc = wpc_of<KIND>();
+  uint4 w0[kWpc][kV], w1[kWpc][kV];  // rows g and g + 8
+  uint32_t s0[kWpc], s1[kWpc];         // NVFP4: the two E4M3 scale bytes of the 32-k run
+  float f0[kWpc][2], f1[kWpc][2];      // FP8: the two float scales of the 32-k run
+};
+
+template <int DT, int KIND>
+__device__ __forceinline__ void chunk_load(Chunk<DT, KIND>& c, const FastParams& p, int row0,
+                                           int row1, int win_begin, int win_end, int t) {
+  constexpr int kWpc = wpc_of<KIND>();
+  const int S = (p.K + (1 << p.bs_shift) - 1) >> p.bs_shift;
+#pragma unroll
+  for (int i = 0; i < kWpc; ++i) {
+    const int w = win_begin + i;
+    const int k0 = w * 128 + 32 * t;
+    const bool kin = (w < win_end) && (k0 < p.K);
+    const bool v0 = kin && row0 < p.N, v1 = kin && row1 < p.N;
+#pragma unroll
+    for (int v = 0; v < Chunk<DT, KIND>::kV; ++v) {
+      c.w0[i][v] = make_uint4(0, 0, 0, 0);
+      c.w1[i][v] = make_uint4(0, 0, 0, 0);
+    }
+    c.s0[i] = c.s1[i] = 0;
+    c.f0[i][0] = c.f0[i][1] = c.f1[i][0] = c.f1[i][1] = 0.f;
+    const int sa = k0 >> p.bs_shift, sb = (k0 + 16) >> p.bs_shift;
+    if constexpr (KIND == 0) {
+      if (v0) {
+        c.w0[i][0] = ldg_stream_v4(p.B + (int64_t)row0 * (p.K / 2) + k0 / 2);
+        const uint8_t* sr = p.ws + (int64_t)row0 * S;
+        c.s0[i] = (uint32_t)__ldg(sr + sa) | ((uint32_t)__ldg(sr + sb) << 8);
+      }
+      if (v1) {
+        c.w1[i][0] = ldg_stream_v4(p.B + (int64_t)row1 * (p.K / 2) + k0 / 2);
+        const uint8_t* sr = p.ws + (int64_t)row1 * S;
+        c.s1[i] = (uint32_t)__ldg(sr + sa) | ((uint32_t)__ldg(sr + sb) << 8);
+      }
+    } else {
+      if (v0) {
+        const uint8_t* r = p.B + (int64_t)row0 * p.K + k0;
+        c.w0[i][0] = ldg_stream_v4(r);
+        c.w0[i][1] = ldg_stream_v4(r + 16);
+        c.f0[i][0] = __ldg(p.fscale + (int64_t)row0 * S + sa);
+        c.f0[i][1] = __ldg(p.fscale + (int64_t)row0 * S + sb);
+      }
+      if (v1) {
+        const uint8_t* r = p.B + (int64_t)row1 * p.K + k0;
+        c.w1[i][0] = ldg_stream_v4(r);
+        c.w1[i][1] = ldg_stream_v4(r + 16);
+        c.f1[i][0] = __ldg(p.fscale + (int64_t)row1 * S + sa);
+        c.f1[i][1] = __ldg(p.fscale + (int64_t)row1 * S + sb);
+      }
+    }
+  }
+}
+
+template <int DT, int KIND>
+__device__ __forceinline__ void chunk_compute(float (&acc)[4], const Chunk<DT, KIND>& c,
+                                              const uint8_t* act_row, bool act_on, int k_lo,
+                                              int win_begin, int win_end, int t) {
+  constexpr int kWpc = wpc_of<KIND>();
+#pragma unroll
+  for (int i = 0; i < kWpc; ++i) {
+    const int w = win_begin + i;
+    if (w >= win_end) break;
+    uint32_t x[16];
+    if (act_on) {
+      const uint4* ap = reinterpret_cast<const uint4*>(act_row + (w * 128 + 32 * t - k_lo) * 2);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = ap[q];
+        x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) x[q] = 0;
+    }
+    if constexpr (KIND == 0) {
+      // f16 scale pairs {s, s} for the two 16-k chunks of each row.
+      const uint32_t h0 = e4m3x2_to_f16x2(c.s0[i]);
+      const uint32_t h1 = e4m3x2_to_f16x2(c.s1[i]);
+      const uint32_t sc0[2] = {__byte_perm(h0, 0, 0x1010), __byte_perm(h0, 0, 0x3232)};
+      const uint32_t sc1[2] = {__byte_perm(h1, 0, 0x1010), __byte_perm(h1, 0, 0x3232)};
+      const uint32_t p0[4] = {c.w0[i][0].x, c.w0[i][0].y, c.w0[i][0].z, c.w0[i][0].w};
+      const uint32_t p1[4] = {c.w1[i][0].x, c.w1[i][0].y, c.w1[i][0].z, c.w1[i][0].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int sh = 16 * (j & 1);
+        const uint32_t b0r = p0[j >> 1] >> sh, b1r = p1[j >> 1] >> sh;
+        const uint32_t a0 = fp4_pair<DT>(b0r & 0xFF, sc0[j >> 2]);
+        const uint32_t a2 = fp4_pair<DT>((b0r >> 8) & 0xFF, sc0[j >> 2]);
+        const uint32_t a1 = fp4_pair<DT>(b1r & 0xFF, sc1[j >> 2]);
+        const uint32_t a3 = fp4_pair<DT>((b1r >> 8) & 0xFF, sc1[j >> 2]);
+        mma_16816(acc, a0, a1, a2, a3, x[2 * j], x[2 * j + 1], DT);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        // bytes 4j .. 4j + 3 of the 32-byte run; chunk j / 4 of 16 k.
+        const uint4 q0 = c.w0[i][j >> 2], q1 = c.w1[i][j >> 2];
+        const uint32_t wv0 = ((const uint32_t*)&q0)[j & 3];
+        const uint32_t wv1 = ((const uint32_t*)&q1)[j & 3];
+        const float sa = c.f0[i][j >> 2], sb = c.f1[i][j >> 2];
+        const uint32_t a0 = fp8_pair<DT>(wv0 & 0xFFFF, sa);
+        const uint32_t a2 = fp8_pair<DT>(wv0 >> 16, sa);
+        const uint32_t a1 = fp8_pair<DT>(wv1 & 0xFFFF, sb);
+        const uint32_t a3 = fp8_pair<DT>(wv1 >> 16, sb);
+        mma_16816(acc, a0, a1, a2, a3, x[2 * j], x[2 * j + 1], DT);
+      }
+    }
+  }
+}
+
+template <int DT, int KIND>
+__global__ void __launch_bounds__(kFastWarps * 32, 2) gemv_fast(const FastParams p) {
+  extern __shared__ __align__(16) uint8_t gsm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int C = gridDim.y;
+  const int rank = blockIdx.y;
+  const int nwin = (p.K + 127) / 128;
+  const int win_lo = rank * p.wpc;
+  const int win_hi = min(win_lo + p.wpc, nwin);
+  const int k_lo = win_lo * 128;
+  const int k_hi = min(win_hi * 128, p.K);
+  const int row0 = blockIdx.x * kFastRows + warp * 16 + g;
+  const int row1 = row0 + 8;
+  uint8_t* act = gsm;
+  float4* red = reinterpret_cast<float4*>(gsm + p.M * p.act_pitch);
+
+  // Cluster peers must be running before any distributed shared-memory store.
+  if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  // L2 prefetch of this lane pair's weight rows (before the dependency wait).
+  if (t == 0 && win_hi > win_lo) {
+    const int wbytes = (KIND == 0) ? (k_hi - k_lo) / 2 : (k_hi - k_lo);
+    const int64_t pitch = (KIND == 0) ? p.K / 2 : p.K;
+    const int64_t off = (KIND == 0) ? k_lo / 2 : k_lo;
+    if (row0 < p.N)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.B + row0 * pitch + off),
+                   "r"(wbytes) : "memory");
+    if (row1 < p.N)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.B + row1 * pitch + off),
+                   "r"(wbytes) : "memory");
+  }
+  pdl_wait();
+
+  Chunk<DT, KIND> c0, c1;
+  chunk_load<DT, KIND>(c0, p, row0, row1, win_lo, win_hi, t);
+
+  // Stage A[:, win_lo*128 .. win_hi*128) in shared memory (zero beyond K).
+  {
+    const int kr = (win_hi - win_lo) * 128;
+    const int vec_per_row = kr / 8;
+    for (int v = threadIdx.x; v < p.M * vec_per_row; v += blockDim.x) {
+      const int m = v / vec_per_row, cv = v - m * vec_per_row;
+      const int k = k_lo + cv * 8;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (k < p.K) val = __ldg(reinterpret_cast<const uint4*>(p.A + (int64_t)m * p.K + k));
+      *reinterpret_cast<uint4*>(act + m * p.act_pitch + cv * 16) = val;
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  constexpr int kWpc = wpc_of<KIND>();
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const bool act_on = g < p.M;
+  const uint8_t* act_row = act + (act_on ? g : 0) * p.act_pitch;
+  for (int wb = win_lo; wb < win_hi; wb += 2 * kWpc) {
+    if (wb + kWpc < win_hi) chunk_load<DT, KIND>(c1, p, row0, row1, wb + kWpc, win_hi, t);
+    chunk_compute<DT, KIND>(acc, c0, act_row, act_on, k_lo, wb, win_hi, t);
+    if (wb + 2 * kWpc < win_hi) chunk_load<DT, KIND>(c0, p, row0, row1, wb + 2 * kWpc, win_hi, t);
+    if (wb + kWpc < win_hi)
+      chunk_compute<DT, KIND>(acc, c1, act_row, act_on, k_lo, wb + kWpc, win_hi, t);
+  }
+
+  if (C > 1) {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    const uint32_t local = smem_u32(red + (rank * kFastWarps + warp) * 32 + lane);
+    st_cluster_f32x4(mapa_shared(local, 0), acc[0], acc[1], acc[2], acc[3]);
+    cluster_sync();
+    if (rank != 0) return;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+    for (int r = 0; r < C; ++r) {
+      const float4 v = red[(r * kFastWarps + warp) * 32 + lane];
+      acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+    }
+  }
+  const float gs = (KIND == 0) ? __ldg(p.gscale) : 1.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = (i < 2) ? row0 : row1;
+    const int m = 2 * t + (i & 1);
+    if (n < p.N && m < p.M) {
+      float y = acc[i] * gs;
+      if (p.bias) y += act_to_f32<DT>(__ldg(p.bias + n));
+      p.Y[(int64_t)m * p.N + n] = to_act_rn<DT>(y);
+    }
+  }
+}
+
+int ilog2(int v) {
+  int s = 0;
+  while ((1 << s) < v) ++s;
+  return (1 << s) == v ? s : -1;
+}
+
+struct FastPlan {
+  int C = 1, wpc = 1, act_pitch = 0;
+  size_t smem = 0;
+};
+
+constexpr size_t kFastSmemLimit = 200 * 1024;
+
+// Cluster size and K split: two CTAs per SM where the column count allows
+// it, the rest of the parallelism from splitting K across up to 8 CTAs, and
+// the activation slice small enough for shared memory.
+bool plan_fast(const GemvArgs& a, FastPlan& pl) {
+  if (a.M < 1 || a.M > 8 || a.K % 32 != 0 || ilog2(a.bs) < 4) return false;
+  if (a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 30)) return false;
+  const DeviceInfo& d = device_info();
+  const int64_t groups = (a.N + kFastRows - 1) / kFastRows;
+  const int nwin = (int)((a.K + 127) / 128);
+  int C = (int)((2 * d.sm_count + groups - 1) / groups);
+  C = std::max(1, std::min(C, std::min(8, nwin)));
+  for (;; ++C) {
+    if (C > std::min(8, nwin)) return false;
+    const int wpc = (nwin + C - 1) / C;
+    const int Ce = (nwin + wpc - 1) / wpc;  // no empty ranks
+    const int pitch = wpc * 256 + 16;
+    const size_t smem = (size_t)a.M * pitch + (Ce > 1 ? (size_t)Ce * kFastWarps * 32 * 16 : 0);
+    if (smem <= kFastSmemLimit) {
+      pl.C = Ce;
+      pl.wpc = wpc;
+      pl.act_pitch = pitch;
+      pl.smem = smem;
+      return true;
+    }
+  }
+}
+
+template <int DT, int KIND>
+int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
+  const int groups = (int)((a.N + kFastRows - 1) / kFastRows);
+  FastParams p;
+  p.A = reinterpret_cast<const uint16_t*>(a.A);
+  p.B = a.B;
+  p.ws = a.ws;
+  p.gscale = a.gscale;
+  p.fscale = a.fscale;
+  p.bias = reinterpret_cast<const uint16_t*>(a.bias);
+  p.Y = reinterpret_cast<uint16_t*>(a.Y);
+  p.M = (int)a.M;
+  p.N = (int)a.N;
+  p.K = (int)a.K;
+  p.bs_shift = ilog2(a.bs);
+  p.wpc = pl.wpc;
+  p.act_pitch = pl.act_pitch;
+  p.err = device_error_word();
+  static std::once_flag once[2][2];
+  std::call_once(once[DT][KIND], [] {
+    cudaFuncSetAttribute(gemv_fast<DT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kFastSmemLimit);
+  });
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)groups, (unsigned)pl.C, 1);
+  cfg.blockDim = dim3(kFastWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)pl.C;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_fast<DT, KIND>, p);
+  return e == cudaSuccess ? kOk : kCuda;
+}
+
 }  // namespace
 
 int launch_gemv(const GemvArgs& a, cudaStream_t st) {
+  FastPlan pl;
+  if (plan_fast(a, pl)) {
+    if (a.kind == 0)
+      return a.dtype == 1 ? launch_fast_t<1, 0>(a, pl, st) : launch_fast_t<0, 0>(a, pl, st);
+    return a.dtype == 1 ? launch_fast_t<1, 1>(a, pl, st) : launch_fast_t<0, 1>(a, pl, st);
+  }
   if (a.kind == 0) {
     return a.dtype == 1 ? launch_general_t<1, 0>(a, st) : launch_general_t<0, 0>(a, st);
   }

@@ -193,17 +193,31 @@ __device__ __forceinline__ uint4 lds_swz(const uint8_t* tile, uint32_t off) {
   return *reinterpret_cast<const uint4*>(tile + phys);
 }
 
-// Decode one packed NVFP4 byte pair-word: 4 bytes (8 codes) with one f16
-// scale -> 4 words of 16-bit operands (DT) holding e2m1 * scale exactly.
+// Decode one packed NVFP4 word (4 bytes, 8 codes) with one block scale
+// (f16 bits, low half) -> 4 words of 16-bit operands (DT) holding
+// e2m1 * scale exactly (at most 6 significant bits).
 template <int DT>
 __device__ __forceinline__ void decode_fp4_word(uint32_t w, uint32_t sc16, uint32_t* out) {
   uint32_t h[4];
   e2m1x8_to_f16x8(w, h);
-  const float sc = __half2float(__ushort_as_half((unsigned short)sc16));
+  if constexpr (DT == 0) {
+    const uint32_t sc2 = __byte_perm(sc16, 0, 0x1010);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 c = f16x2_to_f32x2(h[i]);
-    out[i] = pack2_rn<DT>(c.x * sc, c.y * sc);  // exact products, exact packing
+    for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(h[i]), "r"(sc2));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      asm("{ .reg .b16 l, u, s; .reg .f32 z;\n\t"
+          "mov.b32 {l, u}, %2;\n\t"
+          "cvt.u16.u32 s, %3;\n\t"
+          "mov.f32 z, 0f00000000;\n\t"
+          "fma.rn.f32.f16 %0, l, s, z;\n\t"
+          "fma.rn.f32.f16 %1, u, s, z; }"
+          : "=f"(lo), "=f"(hi)
+          : "r"(h[i]), "r"(sc16));
+      out[i] = pack2_rn<1>(lo, hi);
+    }
   }
 }
 

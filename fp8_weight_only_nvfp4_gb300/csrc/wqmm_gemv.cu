@@ -342,12 +342,10 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One packed NVFP4 byte (in the low 8 bits of `byte`) times an f16 scale ->
-// a 16-bit operand pair (low nibble in the low half).  Exact.
+// A decoded f16x2 E2M1 pair times an f16 scale -> 16-bit operand pair (DT).
+// Exact: the products have at most 6 significant bits.
 template <int DT>
-__device__ __forceinline__ uint32_t fp4_pair(uint32_t byte, uint32_t sc16x2) {
-  uint32_t h;
-  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(h) : "r"(byte));
+__device__ __forceinline__ uint32_t fold_f16x2(uint32_t h, uint32_t sc16x2) {
   if constexpr (DT == 0) {
     uint32_t r;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));
@@ -471,14 +469,19 @@ __device__ __forceinline__ void chunk_compute(float (&acc)[4], const Chunk<DT, K
       const uint32_t p0[4] = {c.w0[i][0].x, c.w0[i][0].y, c.w0[i][0].z, c.w0[i][0].w};
       const uint32_t p1[4] = {c.w1[i][0].x, c.w1[i][0].y, c.w1[i][0].z, c.w1[i][0].w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int sh = 16 * (j & 1);
-        const uint32_t b0r = p0[j >> 1] >> sh, b1r = p1[j >> 1] >> sh;
-        const uint32_t a0 = fp4_pair<DT>(b0r & 0xFF, sc0[j >> 2]);
-        const uint32_t a2 = fp4_pair<DT>((b0r >> 8) & 0xFF, sc0[j >> 2]);
-        const uint32_t a1 = fp4_pair<DT>(b1r & 0xFF, sc1[j >> 2]);
-        const uint32_t a3 = fp4_pair<DT>((b1r >> 8) & 0xFF, sc1[j >> 2]);
-        mma_16816(acc, a0, a1, a2, a3, x[2 * j], x[2 * j + 1], DT);
+      for (int q = 0; q < 4; ++q) {
+        // word q = bytes 4q .. 4q + 3 = MMAs 2q (bytes 4q, 4q+1) and 2q + 1.
+        uint32_t h0[4], h1[4];
+        e2m1x8_to_f16x8(p0[q], h0);
+        e2m1x8_to_f16x8(p1[q], h1);
+        const uint32_t s0 = sc0[q >> 1], s1 = sc1[q >> 1];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = 2 * q + u;
+          mma_16816(acc, fold_f16x2<DT>(h0[2 * u], s0), fold_f16x2<DT>(h1[2 * u], s1),
+                    fold_f16x2<DT>(h0[2 * u + 1], s0), fold_f16x2<DT>(h1[2 * u + 1], s1),
+                    x[2 * j], x[2 * j + 1], DT);
+        }
       }
     } else {
 #pragma unroll
@@ -669,9 +672,324 @@ int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
   return e == cudaSuccess ? kOk : kCuda;
 }
 
+
+// ===========================================================================
+// TMA-fed decode GEMV for NVFP4 with block_size 16 and K % 256 == 0.
+//
+// Same MMA mapping and cluster split-K reduction as gemv_fast, but the bytes
+// in flight live in shared memory instead of registers.  A producer warp
+// streams, per 256-k step, three 2-D tensor copies into a stage ring:
+//   packed weight  [64 rows x 128 B]   8 KB, 128-byte swizzle
+//   block scales   [64 rows x 16 B]    1 KB
+//   activation     [8 rows x 256 k]    4 KB, as four 64-k boxes, 128-byte
+//                                      swizzle (rows >= M are zero-filled)
+// so a CTA keeps up to a whole ring of weight requested at once.  Eight
+// consumer warps decode and multiply: warp w takes 16-row tile (w & 3) and
+// window (w >> 2) of each step, with two independent accumulator chains;
+// the two window halves are added in shared memory, then the cluster ranks.
+// ===========================================================================
+
+constexpr int kTTiles = 4;                  // 16-row tiles per CTA
+constexpr int kTRows = 16 * kTTiles;        // 64 weight rows per CTA
+constexpr int kTCons = 2 * kTTiles;         // consumer warps
+constexpr int kTStepW = kTRows * 128;       // packed bytes per step
+constexpr int kTStepS = kTRows * 16;        // scale bytes per step
+constexpr int kTStepA = 8 * 256 * 2;        // activation bytes per step
+constexpr int kTStage = kTStepW + kTStepA + kTStepS;  // 13 KB (W and A 1024-aligned)
+constexpr int kTMaxStages = 8;
+constexpr int kTThreads = (kTCons + 1) * 32;
+
+struct TmaGemvParams {
+  const float* gscale;
+  const uint16_t* bias;
+  uint16_t* Y;
+  int M, N, K;
+  int spc;        // 256-k steps per cluster rank
+  int nstages;    // ring depth
+  int* err;
+};
+
+struct TmaGemvSmem {
+  int stages, half, red, bars, total;
+  __host__ __device__ TmaGemvSmem(int nstages, int C) {
+    stages = 0;
+    half = stages + nstages * kTStage;
+    red = half + kTTiles * 32 * 16;
+    bars = red + (C > 1 ? C * kTTiles * 32 * 16 : 0);
+    total = bars + 2 * kTMaxStages * 8 + 16;
+  }
+};
+
+__device__ __forceinline__ bool wait_abortable(uint64_t* bar, uint32_t parity, int* err,
+                                               volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  record_error(err, kTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CUtensorMap tmW,
+                                                      const __grid_constant__ CUtensorMap tmS,
+                                                      const __grid_constant__ CUtensorMap tmA,
+                                                      const TmaGemvParams p) {
+  extern __shared__ uint8_t gsm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int C = gridDim.y;
+  const int rank = blockIdx.y;
+  const TmaGemvSmem L(p.nstages, C);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* empty = full + kTMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kTMaxStages);
+  float4* half = reinterpret_cast<float4*>(sm + L.half);
+  float4* red = reinterpret_cast<float4*>(sm + L.red);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int nsteps = p.K / 256;
+  const int s_lo = rank * p.spc;
+  const int s_hi = min(s_lo + p.spc, nsteps);
+  const int nst = s_hi - s_lo;
+  const int row_base = blockIdx.x * kTRows;
+  const int NS = p.nstages;
+  const int tile = warp & (kTTiles - 1);
+  const int hw = warp >> 2;  // which 128-k window of each step
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kTCons);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  __syncthreads();
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+
+  if (warp == kTCons) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tmW);
+      prefetch_tmap(&tmS);
+      prefetch_tmap(&tmA);
+      for (int i = 0; i < nst; ++i) {
+        tma_prefetch_2d(&tmW, (s_lo + i) * 128, row_base);
+        tma_prefetch_2d(&tmS, (s_lo + i) * 16, row_base);
+      }
+      pdl_wait();
+      int issued = 0;
+      for (int i = 0; i < nst; ++i) {
+        const int st = i % NS;
+        if (i >= NS && !wait_abortable(&empty[st], ((i / NS) + 1) & 1, p.err, abort_flag)) break;
+        uint8_t* base = sm + L.stages + st * kTStage;
+        mbar_arrive_expect_tx(&full[st], kTStage);
+        tma_load_2d(base, &tmW, (s_lo + i) * 128, row_base, &full[st]);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          tma_load_2d(base + kTStepW + b * 1024, &tmA, (s_lo + i) * 256 + 64 * b, 0, &full[st]);
+        tma_load_2d(base + kTStepW + kTStepA, &tmS, (s_lo + i) * 16, row_base, &full[st]);
+        ++issued;
+      }
+      for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i) {
+        const uint32_t a = smem_u32(&full[i % NS]);
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+          if (mbar_try_wait(a, (i / NS) & 1)) break;
+          if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+  } else {
+    // ---------------- consumers ----------------
+    const bool act_on = g < p.M;
+    const int r0 = tile * 16 + g, r1 = r0 + 8;  // rows within the CTA
+    for (int i = 0; i < nst; ++i) {
+      const int st = i % NS;
+      if (!wait_abortable(&full[st], (i / NS) & 1, p.err, abort_flag)) break;
+      if (i == 0) pdl_launch_dependents();
+      const uint8_t* wt = sm + L.stages + st * kTStage;
+      const uint8_t* at = wt + kTStepW;
+      const uint8_t* sct = at + kTStepA;
+      const uint32_t off0 = r0 * 128 + 64 * hw + 16 * t;
+      const uint32_t off1 = r1 * 128 + 64 * hw + 16 * t;
+      const uint4 pw0 = *reinterpret_cast<const uint4*>(wt + (off0 ^ ((r0 & 7) << 4)));
+      const uint4 pw1 = *reinterpret_cast<const uint4*>(wt + (off1 ^ ((r1 & 7) << 4)));
+      const uint32_t sb0 = *reinterpret_cast<const uint16_t*>(sct + r0 * 16 + 8 * hw + 2 * t);
+      const uint32_t sb1 = *reinterpret_cast<const uint16_t*>(sct + r1 * 16 + 8 * hw + 2 * t);
+      uint32_t x[16];
+      if (act_on) {
+        // k = 128 hw + 32 t .. +32 lives in 64-k box (2 hw + t / 2), 64 bytes
+        // into row g (16-byte chunks swizzled by g).
+        const uint8_t* box = at + (2 * hw + (t >> 1)) * 1024 + g * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = 4 * (t & 1) + q;
+          const uint4 v = *reinterpret_cast<const uint4*>(box + ((c ^ g) << 4));
+          x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) x[q] = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);  // operands are in registers now
+      const uint32_t h0 = e4m3x2_to_f16x2(sb0);
+      const uint32_t h1 = e4m3x2_to_f16x2(sb1);
+      const uint32_t sc0[2] = {__byte_perm(h0, 0, 0x1010), __byte_perm(h0, 0, 0x3232)};
+      const uint32_t sc1[2] = {__byte_perm(h1, 0, 0x1010), __byte_perm(h1, 0, 0x3232)};
+      const uint32_t p0[4] = {pw0.x, pw0.y, pw0.z, pw0.w};
+      const uint32_t p1[4] = {pw1.x, pw1.y, pw1.z, pw1.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t h0[4], h1[4];
+        e2m1x8_to_f16x8(p0[q], h0);
+        e2m1x8_to_f16x8(p1[q], h1);
+        const uint32_t s0 = sc0[q >> 1], s1 = sc1[q >> 1];
+        const int j0 = 2 * q, j1 = 2 * q + 1;
+        mma_16816(acc, fold_f16x2<DT>(h0[0], s0), fold_f16x2<DT>(h1[0], s1),
+                  fold_f16x2<DT>(h0[1], s0), fold_f16x2<DT>(h1[1], s1), x[2 * j0], x[2 * j0 + 1],
+                  DT);
+        mma_16816(acc2, fold_f16x2<DT>(h0[2], s0), fold_f16x2<DT>(h1[2], s1),
+                  fold_f16x2<DT>(h0[3], s0), fold_f16x2<DT>(h1[3], s1), x[2 * j1], x[2 * j1 + 1],
+                  DT);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+    // Add the two window halves: warps 4..7 hand their sums to warps 0..3.
+    if (hw == 1) half[tile * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    asm volatile("bar.sync 1, %0;" ::"n"(kTCons * 32) : "memory");
+    if (hw == 0) {
+      const float4 v = half[tile * 32 + lane];
+      acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+    }
+  }
+
+  // Cross-CTA reduction (rank order) and epilogue by rank 0's first four warps.
+  __syncwarp();  // the producer warp reconverges before the .aligned cluster barriers
+  const bool owner = warp < kTTiles;
+  if (C > 1) {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (owner) {
+      const uint32_t local = smem_u32(red + (rank * kTTiles + warp) * 32 + lane);
+      st_cluster_f32x4(mapa_shared(local, 0), acc[0], acc[1], acc[2], acc[3]);
+    }
+    cluster_sync();
+    if (rank != 0 || !owner) return;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+    for (int r = 0; r < C; ++r) {
+      const float4 v = red[(r * kTTiles + warp) * 32 + lane];
+      acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+    }
+  } else if (!owner) {
+    return;
+  }
+  const int row0 = row_base + tile * 16 + g;
+  const int row1 = row0 + 8;
+  const float gs = __ldg(p.gscale);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = (i < 2) ? row0 : row1;
+    const int m = 2 * t + (i & 1);
+    if (n < p.N && m < p.M) {
+      float y = acc[i] * gs;
+      if (p.bias) y += act_to_f32<DT>(__ldg(p.bias + n));
+      p.Y[(int64_t)m * p.N + n] = to_act_rn<DT>(y);
+    }
+  }
+}
+
+struct TmaPlan {
+  int C = 1, spc = 1, nstages = 1;
+  size_t smem = 0;
+};
+
+bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
+  if (a.kind != 0 || a.bs != 16 || a.K % 256 != 0 || a.M < 1 || a.M > 8) return false;
+  if (a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 30)) return false;
+  const DeviceInfo& d = device_info();
+  const int64_t groups = (a.N + kTRows - 1) / kTRows;
+  const int nsteps = (int)(a.K / 256);
+  int C = (int)((2 * d.sm_count + groups - 1) / groups);
+  C = std::max(1, std::min(C, std::min(8, nsteps)));
+  const int spc = (nsteps + C - 1) / C;
+  C = (nsteps + spc - 1) / spc;
+  const int ns = std::min(spc, 4);  // ~63 KB per CTA: three CTAs per SM
+  const TmaGemvSmem L(ns, C);
+  pl.C = C;
+  pl.spc = spc;
+  pl.nstages = ns;
+  pl.smem = (size_t)L.total + 1024;
+  return pl.smem <= kFastSmemLimit;
+}
+
+template <int DT>
+int launch_tma_t(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
+  CUtensorMap tmW, tmS, tmA;
+  const uint64_t S = (uint64_t)a.K / 16;
+  const CUtensorMapDataType adt =
+      DT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, (uint64_t)a.K / 2, (uint64_t)a.N,
+                      (uint64_t)a.K / 2, 128, kTRows, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_tmap_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ws, S, (uint64_t)a.N, S, 16, kTRows,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_tmap_2d(&tmA, adt, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64, 8,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    return kCuda;
+  TmaGemvParams p;
+  p.gscale = a.gscale;
+  p.bias = reinterpret_cast<const uint16_t*>(a.bias);
+  p.Y = reinterpret_cast<uint16_t*>(a.Y);
+  p.M = (int)a.M;
+  p.N = (int)a.N;
+  p.K = (int)a.K;
+  p.spc = pl.spc;
+  p.nstages = pl.nstages;
+  p.err = device_error_word();
+  static std::once_flag once[2];
+  std::call_once(once[DT], [] {
+    cudaFuncSetAttribute(gemv_tma<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kFastSmemLimit);
+  });
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.N + kTRows - 1) / kTRows), (unsigned)pl.C, 1);
+  cfg.blockDim = dim3(kTThreads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)pl.C;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tma<DT>, tmW, tmS, tmA, p);
+  return e == cudaSuccess ? kOk : kCuda;
+}
+
 }  // namespace
 
 int launch_gemv(const GemvArgs& a, cudaStream_t st) {
+  TmaPlan tp;
+  if (plan_tma(a, tp))
+    return a.dtype == 1 ? launch_tma_t<1>(a, tp, st) : launch_tma_t<0>(a, tp, st);
   FastPlan pl;
   if (plan_fast(a, pl)) {
     if (a.kind == 0)

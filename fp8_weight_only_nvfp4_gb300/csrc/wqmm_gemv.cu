@@ -346,15 +346,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // Exact: the products have at most 6 significant bits.
 template <int DT>
 __device__ __forceinline__ uint32_t fold_f16x2(uint32_t h, uint32_t sc16x2) {
-  if constexpr (DT == 0) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));
-    return r;
-  } else {
-    float lo, hi;
-    fold_pair_f16(h, sc16x2 & 0xFFFFu, lo, hi);
-    return pack2_rn<1>(lo, hi);
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));  // exact
+  if constexpr (DT == 1) {
+    const float2 f = f16x2_to_f32x2(r);                                // exact
+    r = pack2_rn<1>(f.x, f.y);                                          // exact
   }
+  return r;
 }
 
 // FP8: two E4M3 bytes (low 16 bits) times a float scale -> operand pair,
@@ -676,26 +674,27 @@ int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
 // ===========================================================================
 // TMA-fed decode GEMV for NVFP4 with block_size 16 and K % 256 == 0.
 //
-// Same MMA mapping and cluster split-K reduction as gemv_fast, but the bytes
-// in flight live in shared memory instead of registers.  A producer warp
-// streams, per 256-k step, three 2-D tensor copies into a stage ring:
+// Same MMA mapping as gemv_fast, with the bytes in flight held in shared
+// memory instead of registers.  A producer warp streams, per 256-k step,
+// three 2-D tensor copies into a stage ring:
 //   packed weight  [64 rows x 128 B]   8 KB, 128-byte swizzle
+//   activation     [M rows x 256 k]    four 64-k boxes, 128-byte swizzle
 //   block scales   [64 rows x 16 B]    1 KB
-//   activation     [8 rows x 256 k]    4 KB, as four 64-k boxes, 128-byte
-//                                      swizzle (rows >= M are zero-filled)
-// so a CTA keeps up to a whole ring of weight requested at once.  Eight
-// consumer warps decode and multiply: warp w takes 16-row tile (w & 3) and
-// window (w >> 2) of each step, with two independent accumulator chains;
-// the two window halves are added in shared memory, then the cluster ranks.
+// Four consumer warps, one 16-row MMA tile each, decode and multiply whole
+// steps (both 128-k windows), alternating two accumulator chains.  Waits
+// block with a suspend-time hint instead of spinning.  A thread-block
+// cluster of C CTAs along gridDim.y splits K; after a cluster barrier every
+// rank writes its partial sums into rank 0's (now idle) stage memory and
+// rank 0 adds them in rank order: deterministic, no global scratch.
 // ===========================================================================
 
-constexpr int kTTiles = 4;                  // 16-row tiles per CTA
+constexpr int kTTiles = 4;                  // 16-row tiles (= consumer warps) per CTA
 constexpr int kTRows = 16 * kTTiles;        // 64 weight rows per CTA
-constexpr int kTCons = 2 * kTTiles;         // consumer warps
+constexpr int kTCons = kTTiles;             // consumer warps
 constexpr int kTStepW = kTRows * 128;       // packed bytes per step
+constexpr int kTStepA = 4 * 1024;           // activation boxes (1024-aligned each)
 constexpr int kTStepS = kTRows * 16;        // scale bytes per step
-constexpr int kTStepA = 8 * 256 * 2;        // activation bytes per step
-constexpr int kTStage = kTStepW + kTStepA + kTStepS;  // 13 KB (W and A 1024-aligned)
+constexpr int kTStage = kTStepW + kTStepA + kTStepS;  // 13 KB
 constexpr int kTMaxStages = 8;
 constexpr int kTThreads = (kTCons + 1) * 32;
 
@@ -710,27 +709,36 @@ struct TmaGemvParams {
 };
 
 struct TmaGemvSmem {
-  int stages, half, red, bars, total;
-  __host__ __device__ TmaGemvSmem(int nstages, int C) {
+  int stages, bars, total;
+  __host__ __device__ TmaGemvSmem(int nstages) {
     stages = 0;
-    half = stages + nstages * kTStage;
-    red = half + kTTiles * 32 * 16;
-    bars = red + (C > 1 ? C * kTTiles * 32 * 16 : 0);
+    bars = stages + nstages * kTStage;
     total = bars + 2 * kTMaxStages * 8 + 16;
   }
 };
 
+// Blocking, bounded wait: try_wait with a suspend-time hint parks the warp
+// until the phase completes (or the hint expires) instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool wait_abortable(uint64_t* bar, uint32_t parity, int* err,
                                                volatile int* abort_flag) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_try_wait_sleep(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
   record_error(err, kTimeout);
   *abort_flag = 1;
@@ -747,12 +755,10 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CU
                                            ~uintptr_t(1023));
   const int C = gridDim.y;
   const int rank = blockIdx.y;
-  const TmaGemvSmem L(p.nstages, C);
+  const TmaGemvSmem L(p.nstages);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + kTMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kTMaxStages);
-  float4* half = reinterpret_cast<float4*>(sm + L.half);
-  float4* red = reinterpret_cast<float4*>(sm + L.red);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -762,8 +768,7 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CU
   const int nst = s_hi - s_lo;
   const int row_base = blockIdx.x * kTRows;
   const int NS = p.nstages;
-  const int tile = warp & (kTTiles - 1);
-  const int hw = warp >> 2;  // which 128-k window of each step
+  const uint32_t a_bytes = (uint32_t)p.M * 512u;  // activation bytes per step
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -777,114 +782,128 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CU
   __syncthreads();
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 
   if (warp == kTCons) {
     // ---------------- producer ----------------
+    // Before the dependency wait: pull the first stages' weight and scale
+    // tiles into L2 (prefetches return no data, so they are safe even while
+    // an earlier kernel in the stream still runs).  Only the first ring's
+    // worth: prefetching a long K-range ahead would evict itself from L2.
+    if (lane == 0) {
+      const int npf = min(nst, NS + 2);
+      for (int i = 0; i < npf; ++i) {
+        tma_prefetch_2d(&tmW, (s_lo + i) * 128, row_base);
+        tma_prefetch_2d(&tmS, (s_lo + i) * 16, row_base);
+      }
+    }
     if (lane == 0) {
       prefetch_tmap(&tmW);
       prefetch_tmap(&tmS);
       prefetch_tmap(&tmA);
-      for (int i = 0; i < nst; ++i) {
-        tma_prefetch_2d(&tmW, (s_lo + i) * 128, row_base);
-        tma_prefetch_2d(&tmS, (s_lo + i) * 16, row_base);
-      }
       pdl_wait();
-      int issued = 0;
+      int issued = 0, st = 0;
+      uint32_t ph = 0;
       for (int i = 0; i < nst; ++i) {
-        const int st = i % NS;
-        if (i >= NS && !wait_abortable(&empty[st], ((i / NS) + 1) & 1, p.err, abort_flag)) break;
+        if (i >= NS && !wait_abortable(&empty[st], ph ^ 1u, p.err, abort_flag)) break;
         uint8_t* base = sm + L.stages + st * kTStage;
-        mbar_arrive_expect_tx(&full[st], kTStage);
+        mbar_arrive_expect_tx(&full[st], kTStepW + kTStepS + a_bytes);
         tma_load_2d(base, &tmW, (s_lo + i) * 128, row_base, &full[st]);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
           tma_load_2d(base + kTStepW + b * 1024, &tmA, (s_lo + i) * 256 + 64 * b, 0, &full[st]);
         tma_load_2d(base + kTStepW + kTStepA, &tmS, (s_lo + i) * 16, row_base, &full[st]);
         ++issued;
+        if (++st == NS) { st = 0; ph ^= 1u; }
       }
+      // No copy may still be landing when the CTA moves on or exits.
       for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i) {
         const uint32_t a = smem_u32(&full[i % NS]);
         const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 1;; ++it) {
-          if (mbar_try_wait(a, (i / NS) & 1)) break;
-          if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        while (!mbar_try_wait_sleep(a, (i / NS) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
       }
     }
   } else {
     // ---------------- consumers ----------------
-    const bool act_on = g < p.M;
+    // Lanes g >= M read activation row (g mod M): those MMA columns feed only
+    // outputs m >= M, which are never stored.
+    const int tile = warp;
     const int r0 = tile * 16 + g, r1 = r0 + 8;  // rows within the CTA
+    const int ga = g < p.M ? g : g % p.M;
+    uint32_t w_off[2][2], s_off[2][2], a_off[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      w_off[h][0] = (r0 * 128 + 64 * h + 16 * t) ^ ((r0 & 7) << 4);
+      w_off[h][1] = (r1 * 128 + 64 * h + 16 * t) ^ ((r1 & 7) << 4);
+      s_off[h][0] = kTStepW + kTStepA + r0 * 16 + 8 * h + 2 * t;
+      s_off[h][1] = kTStepW + kTStepA + r1 * 16 + 8 * h + 2 * t;
+      a_off[h] = kTStepW + (2 * h + (t >> 1)) * 1024 + ga * 128;
+    }
+    const uint32_t a_c0 = 4 * (t & 1);
+    const uint32_t a_sw = (uint32_t)(ga & 7);
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    int st = 0;
+    uint32_t ph = 0;
     for (int i = 0; i < nst; ++i) {
-      const int st = i % NS;
-      if (!wait_abortable(&full[st], (i / NS) & 1, p.err, abort_flag)) break;
-      if (i == 0) pdl_launch_dependents();
-      const uint8_t* wt = sm + L.stages + st * kTStage;
-      const uint8_t* at = wt + kTStepW;
-      const uint8_t* sct = at + kTStepA;
-      const uint32_t off0 = r0 * 128 + 64 * hw + 16 * t;
-      const uint32_t off1 = r1 * 128 + 64 * hw + 16 * t;
-      const uint4 pw0 = *reinterpret_cast<const uint4*>(wt + (off0 ^ ((r0 & 7) << 4)));
-      const uint4 pw1 = *reinterpret_cast<const uint4*>(wt + (off1 ^ ((r1 & 7) << 4)));
-      const uint32_t sb0 = *reinterpret_cast<const uint16_t*>(sct + r0 * 16 + 8 * hw + 2 * t);
-      const uint32_t sb1 = *reinterpret_cast<const uint16_t*>(sct + r1 * 16 + 8 * hw + 2 * t);
-      uint32_t x[16];
-      if (act_on) {
-        // k = 128 hw + 32 t .. +32 lives in 64-k box (2 hw + t / 2), 64 bytes
-        // into row g (16-byte chunks swizzled by g).
-        const uint8_t* box = at + (2 * hw + (t >> 1)) * 1024 + g * 128;
+      if (!wait_abortable(&full[st], ph, p.err, abort_flag)) break;
+      const uint8_t* stage = sm + L.stages + st * kTStage;
+      uint4 pw[2][2];
+      uint32_t sb[2][2];
+      uint32_t x[2][16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        pw[h][0] = *reinterpret_cast<const uint4*>(stage + w_off[h][0]);
+        pw[h][1] = *reinterpret_cast<const uint4*>(stage + w_off[h][1]);
+        sb[h][0] = *reinterpret_cast<const uint16_t*>(stage + s_off[h][0]);
+        sb[h][1] = *reinterpret_cast<const uint16_t*>(stage + s_off[h][1]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int c = 4 * (t & 1) + q;
-          const uint4 v = *reinterpret_cast<const uint4*>(box + ((c ^ g) << 4));
-          x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(stage + a_off[h] + (((a_c0 + q) ^ a_sw) << 4));
+          x[h][4 * q] = v.x; x[h][4 * q + 1] = v.y; x[h][4 * q + 2] = v.z; x[h][4 * q + 3] = v.w;
         }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) x[q] = 0;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);  // operands are in registers now
-      const uint32_t h0 = e4m3x2_to_f16x2(sb0);
-      const uint32_t h1 = e4m3x2_to_f16x2(sb1);
-      const uint32_t sc0[2] = {__byte_perm(h0, 0, 0x1010), __byte_perm(h0, 0, 0x3232)};
-      const uint32_t sc1[2] = {__byte_perm(h1, 0, 0x1010), __byte_perm(h1, 0, 0x3232)};
-      const uint32_t p0[4] = {pw0.x, pw0.y, pw0.z, pw0.w};
-      const uint32_t p1[4] = {pw1.x, pw1.y, pw1.z, pw1.w};
+      if (++st == NS) { st = 0; ph ^= 1u; }
+      if (i == 0) pdl_launch_dependents();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t h0[4], h1[4];
-        e2m1x8_to_f16x8(p0[q], h0);
-        e2m1x8_to_f16x8(p1[q], h1);
-        const uint32_t s0 = sc0[q >> 1], s1 = sc1[q >> 1];
-        const int j0 = 2 * q, j1 = 2 * q + 1;
-        mma_16816(acc, fold_f16x2<DT>(h0[0], s0), fold_f16x2<DT>(h1[0], s1),
-                  fold_f16x2<DT>(h0[1], s0), fold_f16x2<DT>(h1[1], s1), x[2 * j0], x[2 * j0 + 1],
-                  DT);
-        mma_16816(acc2, fold_f16x2<DT>(h0[2], s0), fold_f16x2<DT>(h1[2], s1),
-                  fold_f16x2<DT>(h0[3], s0), fold_f16x2<DT>(h1[3], s1), x[2 * j1], x[2 * j1 + 1],
-                  DT);
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t h0 = e4m3x2_to_f16x2(sb[h][0]);
+        const uint32_t h1 = e4m3x2_to_f16x2(sb[h][1]);
+        const uint32_t sc0[2] = {__byte_perm(h0, 0, 0x1010), __byte_perm(h0, 0, 0x3232)};
+        const uint32_t sc1[2] = {__byte_perm(h1, 0, 0x1010), __byte_perm(h1, 0, 0x3232)};
+        const uint32_t p0[4] = {pw[h][0].x, pw[h][0].y, pw[h][0].z, pw[h][0].w};
+        const uint32_t p1[4] = {pw[h][1].x, pw[h][1].y, pw[h][1].z, pw[h][1].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t e0[4], e1[4];
+          e2m1x8_to_f16x8(p0[q], e0);
+          e2m1x8_to_f16x8(p1[q], e1);
+          const uint32_t s0 = sc0[q >> 1], s1 = sc1[q >> 1];
+          const int j0 = 2 * q, j1 = 2 * q + 1;
+          mma_16816(acc, fold_f16x2<DT>(e0[0], s0), fold_f16x2<DT>(e1[0], s1),
+                    fold_f16x2<DT>(e0[1], s0), fold_f16x2<DT>(e1[1], s1), x[h][2 * j0],
+                    x[h][2 * j0 + 1], DT);
+          mma_16816(acc2, fold_f16x2<DT>(e0[2], s0), fold_f16x2<DT>(e1[2], s1),
+                    fold_f16x2<DT>(e0[3], s0), fold_f16x2<DT>(e1[3], s1), x[h][2 * j1],
+                    x[h][2 * j1 + 1], DT);
+        }
       }
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
-    // Add the two window halves: warps 4..7 hand their sums to warps 0..3.
-    if (hw == 1) half[tile * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    asm volatile("bar.sync 1, %0;" ::"n"(kTCons * 32) : "memory");
-    if (hw == 0) {
-      const float4 v = half[tile * 32 + lane];
-      acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
-    }
   }
 
-  // Cross-CTA reduction (rank order) and epilogue by rank 0's first four warps.
+  // Cross-CTA reduction (rank order) into rank 0's idle stage memory.
   __syncwarp();  // the producer warp reconverges before the .aligned cluster barriers
-  const bool owner = warp < kTTiles;
+  const bool owner = warp < kTCons;
   if (C > 1) {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    float4* red = reinterpret_cast<float4*>(sm + L.stages);
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // peers are running
+    cluster_sync();                                              // every ring is drained
     if (owner) {
-      const uint32_t local = smem_u32(red + (rank * kTTiles + warp) * 32 + lane);
+      const uint32_t local = smem_u32(red + (rank * kTCons + warp) * 32 + lane);
       st_cluster_f32x4(mapa_shared(local, 0), acc[0], acc[1], acc[2], acc[3]);
     }
     cluster_sync();
@@ -892,13 +911,13 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CU
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = 0.f;
     for (int r = 0; r < C; ++r) {
-      const float4 v = red[(r * kTTiles + warp) * 32 + lane];
+      const float4 v = red[(r * kTCons + warp) * 32 + lane];
       acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
     }
   } else if (!owner) {
     return;
   }
-  const int row0 = row_base + tile * 16 + g;
+  const int row0 = row_base + warp * 16 + g;
   const int row1 = row0 + 8;
   const float gs = __ldg(p.gscale);
 #pragma unroll
@@ -918,20 +937,78 @@ struct TmaPlan {
   size_t smem = 0;
 };
 
+// Cluster size: among K splits that keep every cluster of the launch
+// resident at once (one wave, from the occupancy query), the one whose CTA
+// count fills the SMs most evenly, at least two steps per rank.  With many
+// column groups, one rank per group keeps every CTA long-lived.
+template <int DT>
+__global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CUtensorMap tmW,
+                                                      const __grid_constant__ CUtensorMap tmS,
+                                                      const __grid_constant__ CUtensorMap tmA,
+                                                      const TmaGemvParams p);
+
+int max_active_clusters(int dt, int C, size_t smem) {
+  static std::mutex mu;
+  static int cache[2][9][8] = {};  // [dt][C][nstages] (0 = unknown)
+  const int ns = (int)((smem - 1024 - 2 * kTMaxStages * 8 - 16) / kTStage);
+  if (ns < 1 || ns > 7 || C < 1 || C > 8) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int& v = cache[dt][C][ns];
+  if (v) return v;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1024, (unsigned)C, 1);
+  cfg.blockDim = dim3(kTThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)C;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const void* fn = dt == 1 ? (const void*)gemv_tma<1> : (const void*)gemv_tma<0>;
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFastSmemLimit);
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+  cudaGetLastError();
+  v = n > 0 ? n : -1;
+  return v;
+}
+
 bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
   if (a.kind != 0 || a.bs != 16 || a.K % 256 != 0 || a.M < 1 || a.M > 8) return false;
   if (a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 30)) return false;
   const DeviceInfo& d = device_info();
   const int64_t groups = (a.N + kTRows - 1) / kTRows;
   const int nsteps = (int)(a.K / 256);
-  int C = (int)((2 * d.sm_count + groups - 1) / groups);
-  C = std::max(1, std::min(C, std::min(8, nsteps)));
-  const int spc = (nsteps + C - 1) / C;
-  C = (nsteps + spc - 1) / spc;
-  const int ns = std::min(spc, 4);  // ~63 KB per CTA: three CTAs per SM
-  const TmaGemvSmem L(ns, C);
-  pl.C = C;
-  pl.spc = spc;
+  int best_C = 1, best_spc = nsteps;
+  double best = -1.0;
+  for (int c = 1; c <= 8 && c <= nsteps; ++c) {
+    const int spc = (nsteps + c - 1) / c;
+    const int ce = (nsteps + spc - 1) / spc;
+    if (ce != c) continue;
+    if (c > 1 && spc < 2) continue;
+    if (groups >= 4 * d.sm_count && c > 1) continue;
+    const int64_t ctas = groups * ce;
+    const int64_t per_sm = (ctas + d.sm_count - 1) / d.sm_count;
+    double eff = (double)ctas / (double)(per_sm * d.sm_count);
+    if (ctas < 2 * d.sm_count) eff *= (double)ctas / (2.0 * d.sm_count);
+    if (groups < 4 * d.sm_count) {
+      const int ns = std::min(spc, 4);
+      const int mac = max_active_clusters(a.dtype == 1 ? 1 : 0, ce,
+                                          (size_t)TmaGemvSmem(ns).total + 1024);
+      if (mac > 0 && groups > mac) eff *= 0.5;  // a second wave of clusters
+    }
+    if (eff > best + 1e-9) {
+      best = eff;
+      best_C = ce;
+      best_spc = spc;
+    }
+  }
+  const int ns = std::min(best_spc, 4);
+  const TmaGemvSmem L(ns);
+  pl.C = best_C;
+  pl.spc = best_spc;
   pl.nstages = ns;
   pl.smem = (size_t)L.total + 1024;
   return pl.smem <= kFastSmemLimit;
@@ -948,8 +1025,9 @@ int launch_tma_t(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_tmap_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ws, S, (uint64_t)a.N, S, 16, kTRows,
                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_tmap_2d(&tmA, adt, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64, 8,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+      !encode_tmap_2d(&tmA, adt, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64,
+                      (uint32_t)a.M, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return kCuda;
   TmaGemvParams p;
   p.gscale = a.gscale;

@@ -19,12 +19,15 @@
 //   warp 1     TMEM owner and MMA issuer (one elected thread):
 //              tcgen05.mma.kind::f16, A = decoded weight from TMEM,
 //              B = activation tile from shared memory, D = FP32 in TMEM;
-//   warps 2-5  decoders: thread i owns weight row i (TMEM lane i); it reads
-//              its packed bytes from shared memory, folds the E4M3 block
-//              scale (exact for NVFP4: <= 6 significant bits, FP4 page §4),
-//              writes the 16-bit operand to TMEM with tcgen05.st, then runs
-//              the epilogue: TMEM -> registers, * gscale, + bias, one RNE,
-//              and stores Y[token, n] (lanes = consecutive n: coalesced).
+//   warps 2-9  decoders: warp w serves TMEM lane quarter (w % 4) and one
+//              half (32 k) of each 64-k stage; thread i of the quarter owns
+//              weight row i (TMEM lane i).  It reads its packed bytes from
+//              shared memory, folds the E4M3 block scale (exact for NVFP4:
+//              <= 6 significant bits, FP4 page §4), writes the 16-bit
+//              operand to TMEM with tcgen05.st, and after the main loop
+//              runs the epilogue for half of the 256 token columns: TMEM ->
+//              registers, * gscale, + bias, one RNE, stores Y[token, n]
+//              (lanes = consecutive n: coalesced).
 //
 // The weight being the MMA A operand is the FP4 page §4 idea (weight in the
 // A slot, activation in the B slot) carried to tcgen05: the decoded weight
@@ -46,7 +49,8 @@ constexpr int kBM = 128;       // weight rows per tile (MMA M)
 constexpr int kBN = 256;       // tokens per tile (MMA N)
 constexpr int kBK = 64;        // k per stage
 constexpr int kStages = 4;
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kDecWarps = 8;   // two per TMEM lane quarter, each half of a stage's k
+constexpr int kThreads = (2 + kDecWarps) * 32;
 constexpr int kActStageBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kWStageBytes = kBM * kBK;         // 8 KB (FP8 worst case; NVFP4 uses 4 KB)
 constexpr int kTmemCols = 512;
@@ -116,6 +120,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
       "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
       "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
@@ -200,23 +213,16 @@ template <int DT>
 __device__ __forceinline__ void decode_fp4_word(uint32_t w, uint32_t sc16, uint32_t* out) {
   uint32_t h[4];
   e2m1x8_to_f16x8(w, h);
-  if constexpr (DT == 0) {
-    const uint32_t sc2 = __byte_perm(sc16, 0, 0x1010);
+  const uint32_t sc2 = __byte_perm(sc16, 0, 0x1010);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(h[i]), "r"(sc2));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float lo, hi;
-      asm("{ .reg .b16 l, u, s; .reg .f32 z;\n\t"
-          "mov.b32 {l, u}, %2;\n\t"
-          "cvt.u16.u32 s, %3;\n\t"
-          "mov.f32 z, 0f00000000;\n\t"
-          "fma.rn.f32.f16 %0, l, s, z;\n\t"
-          "fma.rn.f32.f16 %1, u, s, z; }"
-          : "=f"(lo), "=f"(hi)
-          : "r"(h[i]), "r"(sc16));
-      out[i] = pack2_rn<1>(lo, hi);
+  for (int i = 0; i < 4; ++i) {
+    uint32_t pr;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(pr) : "r"(h[i]), "r"(sc2));  // exact
+    if constexpr (DT == 0) {
+      out[i] = pr;
+    } else {
+      const float2 f = f16x2_to_f32x2(pr);  // exact
+      out[i] = pack2_rn<1>(f.x, f.y);       // exact
     }
   }
 }
@@ -250,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&afull[s], 128);
+      mbar_init(&afull[s], kDecWarps * 32);
     }
     mbar_init(accfull, 1);
     *abort_flag = 0;
@@ -318,18 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- decoders, then epilogue ----------------
     const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int hk = (warp - 2) >> 2;         // which 32-k half of each stage
     const int row = q * 32 + lane;          // weight row within the tile
     const int n = n0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     bool ok = true;
     for (int it = 0; it < num_k; ++it) {
       const int s = it % kStages;
-      // Scales for the four 16-k chunks of this stage (bs is a multiple of 16).
-      uint32_t sc16[4];
-      float scf[4];
+      // Scales of the two 16-k chunks of this half (bs is a multiple of 16).
+      uint32_t sc16[2];
+      float scf[2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int kc = it * kBK + 16 * c;
+      for (int c = 0; c < 2; ++c) {
+        const int kc = it * kBK + 32 * hk + 16 * c;
         sc16[c] = 0;
         scf[c] = 0.f;
         if (n < N && kc < K) {
@@ -342,19 +349,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint8_t* wt = smem + SmemLayout::w + s * kWStageBytes;
-      uint32_t v[32];
+      uint32_t v[16];
       if constexpr (KIND == 0) {
-        // 32 bytes per row, 32-byte swizzle.
-        const uint4 p0 = lds_swz<1>(wt, row * 32);
-        const uint4 p1 = lds_swz<1>(wt, row * 32 + 16);
-        const uint32_t w8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        // 16 bytes (32 k) of this row's 32-byte stage run, 32-byte swizzle.
+        const uint4 p = lds_swz<1>(wt, row * 32 + 16 * hk);
+        const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) decode_fp4_word<DT>(w8[i], sc16[i >> 1], &v[4 * i]);
+        for (int i = 0; i < 4; ++i) decode_fp4_word<DT>(w4[i], sc16[i >> 1], &v[4 * i]);
       } else {
-        // 64 bytes per row, 64-byte swizzle; byte b of the row is k = it*64 + b.
+        // 32 bytes (32 k) of this row's 64-byte stage run, 64-byte swizzle.
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 p = lds_swz<3>(wt, row * 64 + 16 * c);
+        for (int c = 0; c < 2; ++c) {
+          const uint4 p = lds_swz<3>(wt, row * 64 + 32 * hk + 16 * c);
           const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -366,18 +372,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tmem_st32(lane_base + kACol + s * (kBK / 2), v);
+      tmem_st16(lane_base + kACol + s * (kBK / 2) + 16 * hk, v);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&afull[s]);
     }
-    // Epilogue.
+    // Epilogue: this warp's lane quarter, token columns [128 hk, 128 hk + 128).
     if (ok && wait_bar(accfull, 0, err, abort_flag)) {
       tc_fence_after();
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+      for (int c0 = 128 * hk; c0 < 128 * hk + 128; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + kAccCol + c0, r);
         if (n < N) {

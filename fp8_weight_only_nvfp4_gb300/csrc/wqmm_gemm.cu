@@ -19,13 +19,13 @@
 //   warp 1     TMEM owner and MMA issuer (one elected thread):
 //              tcgen05.mma.kind::f16, A = decoded weight from TMEM,
 //              B = activation tile from shared memory, D = FP32 in TMEM;
-//   warps 2-9  decoders: warp w serves TMEM lane quarter (w % 4) and one
-//              half (32 k) of each 64-k stage; thread i of the quarter owns
+//   warps 2-17 decoders: warp w serves TMEM lane quarter (w % 4) and one
+//              quarter (16 k) of each 64-k stage; thread i of the quarter owns
 //              weight row i (TMEM lane i).  It reads its packed bytes from
 //              shared memory, folds the E4M3 block scale (exact for NVFP4:
 //              <= 6 significant bits, FP4 page §4), writes the 16-bit
 //              operand to TMEM with tcgen05.st, and after the main loop
-//              runs the epilogue for half of the 256 token columns: TMEM ->
+//              runs the epilogue for a quarter of the 256 token columns: TMEM ->
 //              registers, * gscale, + bias, one RNE, stores Y[token, n]
 //              (lanes = consecutive n: coalesced).
 //
@@ -49,7 +49,7 @@ constexpr int kBM = 128;       // weight rows per tile (MMA M)
 constexpr int kBN = 256;       // tokens per tile (MMA N)
 constexpr int kBK = 64;        // k per stage
 constexpr int kStages = 4;
-constexpr int kDecWarps = 8;   // two per TMEM lane quarter, each half of a stage's k
+constexpr int kDecWarps = 16;  // four per TMEM lane quarter, each a quarter of a stage's k
 constexpr int kThreads = (2 + kDecWarps) * 32;
 constexpr int kActStageBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kWStageBytes = kBM * kBK;         // 8 KB (FP8 worst case; NVFP4 uses 4 KB)
@@ -129,6 +129,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
       : "memory");
 }
 
@@ -324,66 +331,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- decoders, then epilogue ----------------
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int hk = (warp - 2) >> 2;         // which 32-k half of each stage
+    const int qk = (warp - 2) >> 2;         // which 16-k quarter of each stage
     const int row = q * 32 + lane;          // weight row within the tile
     const int n = n0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     bool ok = true;
     for (int it = 0; it < num_k; ++it) {
       const int s = it % kStages;
-      // Scales of the two 16-k chunks of this half (bs is a multiple of 16).
-      uint32_t sc16[2];
-      float scf[2];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int kc = it * kBK + 32 * hk + 16 * c;
-        sc16[c] = 0;
-        scf[c] = 0.f;
-        if (n < N && kc < K) {
-          if constexpr (KIND == 0)
-            sc16[c] = e4m3x2_to_f16x2(__ldg(ws + (int64_t)n * S + kc / bs)) & 0xFFFFu;
-          else
-            scf[c] = __ldg(fscale + (int64_t)n * S + kc / bs);
-        }
+      // Scale of this 16-k chunk (bs is a multiple of 16).
+      const int kc = it * kBK + 16 * qk;
+      uint32_t sc16 = 0;
+      float scf = 0.f;
+      if (n < N && kc < K) {
+        if constexpr (KIND == 0)
+          sc16 = e4m3x2_to_f16x2(__ldg(ws + (int64_t)n * S + kc / bs)) & 0xFFFFu;
+        else
+          scf = __ldg(fscale + (int64_t)n * S + kc / bs);
       }
       if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint8_t* wt = smem + SmemLayout::w + s * kWStageBytes;
-      uint32_t v[16];
+      uint32_t v[8];
       if constexpr (KIND == 0) {
-        // 16 bytes (32 k) of this row's 32-byte stage run, 32-byte swizzle.
-        const uint4 p = lds_swz<1>(wt, row * 32 + 16 * hk);
+        // 8 bytes (16 k) of this row's 32-byte stage run, 32-byte swizzle.
+        const uint32_t off = row * 32 + 8 * qk;
+        const uint32_t phys = off ^ (((off >> 7) & 1u) << 4);
+        const uint2 pw = *reinterpret_cast<const uint2*>(wt + phys);
+        decode_fp4_word<DT>(pw.x, sc16, &v[0]);
+        decode_fp4_word<DT>(pw.y, sc16, &v[4]);
+      } else {
+        // 16 bytes (16 k) of this row's 64-byte stage run, 64-byte swizzle.
+        const uint4 p = lds_swz<3>(wt, row * 64 + 16 * qk);
         const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) decode_fp4_word<DT>(w4[i], sc16[i >> 1], &v[4 * i]);
-      } else {
-        // 32 bytes (32 k) of this row's 64-byte stage run, 64-byte swizzle.
+        for (int i = 0; i < 4; ++i) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint4 p = lds_swz<3>(wt, row * 64 + 32 * hk + 16 * c);
-          const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float2 e = f16x2_to_f32x2(e4m3x2_to_f16x2((w4[i] >> (16 * h)) & 0xFFFFu));
-              v[8 * c + 2 * i + h] = pack2_rn<DT>(e.x * scf[c], e.y * scf[c]);
-            }
+          for (int h = 0; h < 2; ++h) {
+            const float2 e = f16x2_to_f32x2(e4m3x2_to_f16x2((w4[i] >> (16 * h)) & 0xFFFFu));
+            v[2 * i + h] = pack2_rn<DT>(e.x * scf, e.y * scf);
           }
         }
       }
-      tmem_st16(lane_base + kACol + s * (kBK / 2) + 16 * hk, v);
+      tmem_st8(lane_base + kACol + s * (kBK / 2) + 8 * qk, v);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&afull[s]);
     }
-    // Epilogue: this warp's lane quarter, token columns [128 hk, 128 hk + 128).
+    // Epilogue: this warp's lane quarter, token columns [64 qk, 64 qk + 64).
     if (ok && wait_bar(accfull, 0, err, abort_flag)) {
       tc_fence_after();
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
 #pragma unroll 1
-      for (int c0 = 128 * hk; c0 < 128 * hk + 128; c0 += 32) {
+      for (int c0 = 64 * qk; c0 < 64 * qk + 64; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + kAccCol + c0, r);
         if (n < N) {

@@ -153,6 +153,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise max of per-rank timings (the slowest rank decides)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def weak_scaling_value(per_rank_units, world, seconds):
+    """Whole-job throughput: every rank processed per_rank_units in seconds."""
+    return world * per_rank_units / seconds
+
+
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
@@ -436,6 +451,58 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_only(name, m, reps):
+    """Run one workload a few times (for profilers); prints its device time."""
+    import torch
+    gpu = Gpu("cuda:0")
+    wq = gpu.wq
+    fn = None
+    if name == "gemv":
+        M, N, K = (m or 4), 5120, 5120
+        ly = gpu.fp4_layers(M, N, K, 1, seed0=100)[0]
+        A = gpu.t(wl.gen_activation(M, K, 1, 7).view(np.int16), torch.bfloat16)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+        fn = lambda: wq.fp4_weight_matmul(A, ly["B"], ly["ws"], ly["ws2"], None, 16, out=Y,
+                                          stream=gpu.stream)
+        work = gemv_bytes(M, N, K) / 1e9, "GB/s"
+    elif name == "lm_head":
+        M, N, K = (m or 4), 152064, 5120
+        ly = gpu.fp4_layers(M, N, K, 1, seed0=500, log_uniform=True, ws2=0.01, bias=True)[0]
+        A = gpu.t(wl.gen_activation(M, K, 1, 9).view(np.int16), torch.bfloat16)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+        fn = lambda: wq.fp4_weight_matmul(A, ly["B"], ly["ws"], ly["ws2"], ly["bias"], 16, out=Y,
+                                          stream=gpu.stream)
+        work = gemv_bytes(M, N, K, bias=True) / 1e9, "GB/s"
+    elif name in ("prefill_gate_up", "prefill_down"):
+        M = m or 8192
+        N, K = (17408, 5120) if name == "prefill_gate_up" else (5120, 17408)
+        ly = gpu.fp4_layers(M, N, K, 1, seed0=700, bias=True)[0]
+        A = torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+        fn = lambda: wq.fp4_weight_matmul(A, ly["B"], ly["ws"], ly["ws2"], ly["bias"], 16, out=Y,
+                                          stream=gpu.stream)
+        work = 2 * M * N * K / 1e12, "TFLOP/s"
+    elif name == "dequant":
+        N, K = 17408, 5120
+        ly = gpu.fp4_layers(1, N, K, 1, seed0=700)[0]
+        W = torch.empty(N, K, dtype=torch.bfloat16, device=gpu.dev)
+        fn = lambda: wq.fp4_dequantize(ly["B"], ly["ws"], ly["ws2"], 16, out=W, stream=gpu.stream)
+        work = dequant_bytes(N, K) / 1e9, "GB/s"
+    elif name == "fp8_gemv":
+        M, N, K = (m or 4), 5120, 5120
+        B = gpu.t(wl.gen_fp8_weight(N, K, 300))
+        sc = gpu.t(wl.gen_fp8_scale(N, wl.scale_cols(K, 128), 0.001, 0.02, 300))
+        A = gpu.t(wl.gen_activation(M, K, 1, 7).view(np.int16), torch.bfloat16)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+        fn = lambda: wq.fp8_weight_matmul(A, B, sc, None, 128, out=Y, stream=gpu.stream)
+        work = gemv_bytes(M, N, K, 128, kind="fp8") / 1e9, "GB/s"
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    dt = gpu.time_each(fn, reps=reps, warmup=2, flush=True)
+    print(json.dumps({"only": name, "M": m, "us": round(dt * 1e6, 2),
+                      work[1]: round(work[0] / dt, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,7 +511,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only (no extra workloads)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--only", default=None,
+                    help="run one workload (gemv, lm_head, prefill_gate_up, prefill_down, "
+                         "dequant, fp8_gemv) a few times, for profilers")
+    ap.add_argument("--m", type=int, default=None, help="rows of A for --only")
+    ap.add_argument("--reps", type=int, default=3, help="timed launches for --only")
     args = ap.parse_args()
+    if args.only:
+        run_only(args.only, args.m, args.reps)
+        return
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
@@ -470,14 +545,9 @@ def main():
     peaks = load_peaks()
     h = bench_headline(gpu, args, rank, world, barrier_sync)
     dt = h["dt"]
-    if dist is not None:
-        t = torch.tensor([dt, h["dt_e2e"]], dtype=torch.float64, device=gpu.dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt, dt_e2e = float(t[0]), float(t[1])
-    else:
-        dt_e2e = h["dt_e2e"]
+    dt, dt_e2e = max_over_ranks([dt, h["dt_e2e"]], dist, gpu.dev if dist is not None else None)
     per_step = h["per_launch"] * h["launches"]
-    value = world * per_step * args.steps / dt / 1e9
+    value = weak_scaling_value(per_step * args.steps, world, dt) / 1e9
     avg_launch = dt / (args.steps * h["launches"])
     achieved = h["per_launch"] / avg_launch / 1e9
     line = {
@@ -490,7 +560,8 @@ def main():
                      "traffic": recorded_traffic("gemv_decode_M4_N5120_K5120"),
                      "peak_src": peaks["src"], "algorithmic_bytes_per_launch": h["per_launch"],
                      "avg_launch_us": round(avg_launch * 1e6, 3)},
-        "e2e": {"value": round(world * per_step * args.steps / dt_e2e / 1e9, 1), "unit": UNIT,
+        "e2e": {"value": round(weak_scaling_value(per_step * args.steps, world, dt_e2e) / 1e9, 1),
+                "unit": UNIT,
                 "h2d_bytes_per_step": h["h2d"], "d2h_bytes_per_step": h["d2h"]},
         "gpu_launches": h["launches"] * args.steps,
         "clocks": h["clocks"],

@@ -937,78 +937,31 @@ struct TmaPlan {
   size_t smem = 0;
 };
 
-// Cluster size: among K splits that keep every cluster of the launch
-// resident at once (one wave, from the occupancy query), the one whose CTA
-// count fills the SMs most evenly, at least two steps per rank.  With many
-// column groups, one rank per group keeps every CTA long-lived.
-template <int DT>
-__global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CUtensorMap tmW,
-                                                      const __grid_constant__ CUtensorMap tmS,
-                                                      const __grid_constant__ CUtensorMap tmA,
-                                                      const TmaGemvParams p);
-
-int max_active_clusters(int dt, int C, size_t smem) {
-  static std::mutex mu;
-  static int cache[2][9][8] = {};  // [dt][C][nstages] (0 = unknown)
-  const int ns = (int)((smem - 1024 - 2 * kTMaxStages * 8 - 16) / kTStage);
-  if (ns < 1 || ns > 7 || C < 1 || C > 8) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  int& v = cache[dt][C][ns];
-  if (v) return v;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1024, (unsigned)C, 1);
-  cfg.blockDim = dim3(kTThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = (unsigned)C;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  const void* fn = dt == 1 ? (const void*)gemv_tma<1> : (const void*)gemv_tma<0>;
-  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFastSmemLimit);
-  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
-  cudaGetLastError();
-  v = n > 0 ? n : -1;
-  return v;
-}
-
+// Cluster size: the largest K split (at least two steps per rank) whose CTA
+// count stays within two per SM, so that every CTA is resident at once and
+// the next launch's CTAs still find room to start early (programmatic
+// dependent launch); with many column groups that is one rank per group.
+// Measured on GB300 for N = K = 5120: C = 3 beats 1, 2, 4, 5 and 7.
 bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
   if (a.kind != 0 || a.bs != 16 || a.K % 256 != 0 || a.M < 1 || a.M > 8) return false;
   if (a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 30)) return false;
   const DeviceInfo& d = device_info();
   const int64_t groups = (a.N + kTRows - 1) / kTRows;
   const int nsteps = (int)(a.K / 256);
-  int best_C = 1, best_spc = nsteps;
-  double best = -1.0;
-  for (int c = 1; c <= 8 && c <= nsteps; ++c) {
+  int C = 1;
+  for (int c = 2; c <= 8 && c <= nsteps; ++c) {
     const int spc = (nsteps + c - 1) / c;
+    if (spc < 2) break;
     const int ce = (nsteps + spc - 1) / spc;
-    if (ce != c) continue;
-    if (c > 1 && spc < 2) continue;
-    if (groups >= 4 * d.sm_count && c > 1) continue;
-    const int64_t ctas = groups * ce;
-    const int64_t per_sm = (ctas + d.sm_count - 1) / d.sm_count;
-    double eff = (double)ctas / (double)(per_sm * d.sm_count);
-    if (ctas < 2 * d.sm_count) eff *= (double)ctas / (2.0 * d.sm_count);
-    if (groups < 4 * d.sm_count) {
-      const int ns = std::min(spc, 4);
-      const int mac = max_active_clusters(a.dtype == 1 ? 1 : 0, ce,
-                                          (size_t)TmaGemvSmem(ns).total + 1024);
-      if (mac > 0 && groups > mac) eff *= 0.5;  // a second wave of clusters
-    }
-    if (eff > best + 1e-9) {
-      best = eff;
-      best_C = ce;
-      best_spc = spc;
-    }
+    if (groups * ce > 2 * (int64_t)d.sm_count) break;
+    C = ce;
   }
-  const int ns = std::min(best_spc, 4);
+  const int spc = (nsteps + C - 1) / C;
+  C = (nsteps + spc - 1) / spc;
+  const int ns = std::min(spc, 4);
   const TmaGemvSmem L(ns);
-  pl.C = best_C;
-  pl.spc = best_spc;
+  pl.C = C;
+  pl.spc = spc;
   pl.nstages = ns;
   pl.smem = (size_t)L.total + 1024;
   return pl.smem <= kFastSmemLimit;

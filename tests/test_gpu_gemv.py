@@ -141,3 +141,38 @@ def test_leading_dims():
     assert Y.shape == (2, 3, 32)
     Yr, S = _ref(p)
     assert_within_tolerance(Y.view(6, 32), Yr, S, p.dtype, "3-D A")
+
+
+def _with_activation(p, A):
+    return wl.Fp4Problem(p.M, p.N, p.K, p.block_size, p.dtype, wl.act_bits(A, p.dtype),
+                         p.B_packed, p.weight_scale, p.weight_scale_2, p.bias)
+
+
+def test_bf16_activation_dynamic_range_fallback():
+    """BF16 activations run on FP16 tensor cores after an exact per-row,
+    per-256-k power-of-two rescale; a step whose values span more than 32
+    binades (here 1e30 next to 1e-10) must take the exact BF16 path instead.
+    Other steps of the same rows keep the FP16 path."""
+    M, N, K = 4, 256, 2048
+    p = wl.make_fp4(M, N, K, 16, oracle.BF16, seed=31, bias_sigma=0.1)
+    r = np.random.Generator(np.random.PCG64(5))
+    A = r.standard_normal((M, K))
+    A[1, 300] = 1e30      # step 1 of row 1: huge and ...
+    A[1, 301] = 1e-10     # ... tiny in the same 256-k step
+    A[2, 1024:1280] *= 1e-35  # step 4 of row 2: everything below 2^-111
+    A[3, :] = 0.0             # an all-zero row
+    q = _with_activation(p, A)
+    Yr, S = _ref(q)
+    assert_within_tolerance(run_fp4(q), Yr, S, q.dtype, "dynamic range")
+
+
+def test_bf16_activation_wide_but_exact_range():
+    """Values 2^-30 .. 2^2 inside one step (32 binades) stay on the FP16
+    path and remain exact."""
+    M, N, K = 2, 128, 512
+    p = wl.make_fp4(M, N, K, 16, oracle.BF16, seed=32)
+    r = np.random.Generator(np.random.PCG64(6))
+    A = r.standard_normal((M, K)) * np.exp2(r.integers(-30, 2, size=(M, K)))
+    q = _with_activation(p, A)
+    Yr, S = _ref(q)
+    assert_within_tolerance(run_fp4(q), Yr, S, q.dtype, "wide exact range")

@@ -346,13 +346,19 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // Exact: the products have at most 6 significant bits.
 template <int DT>
 __device__ __forceinline__ uint32_t fold_f16x2(uint32_t h, uint32_t sc16x2) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));  // exact
   if constexpr (DT == 1) {
-    const float2 f = f16x2_to_f32x2(r);                                // exact
-    r = pack2_rn<1>(f.x, f.y);                                          // exact
+    float lo, hi;
+    asm("{ .reg .b16 l, u, s, s2; mov.b32 {l, u}, %2; mov.b32 {s, s2}, %3;\n\t"
+        "fma.rn.f32.f16 %0, l, s, 0f80000000; fma.rn.f32.f16 %1, u, s, 0f80000000; }"
+        : "=f"(lo), "=f"(hi) : "r"(h), "r"(sc16x2));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  } else {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));  // exact
+    return r;
   }
-  return r;
 }
 
 // FP8: two E4M3 bytes (low 16 bits) times a float scale -> operand pair,

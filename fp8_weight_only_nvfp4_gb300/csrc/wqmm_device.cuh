@@ -273,4 +273,23 @@ __device__ __forceinline__ float act_to_f32(uint16_t bits) {
   else return __half2float(__ushort_as_half(bits));
 }
 
+// A decoded f16x2 E2M1 pair times an f16 scale -> 16-bit operand pair (DT).
+// Exact: the products have at most 6 significant bits.
+template <int DT>
+__device__ __forceinline__ uint32_t fold_f16x2(uint32_t h, uint32_t sc16x2) {
+  if constexpr (DT == 1) {
+    float lo, hi;
+    asm("{ .reg .b16 l, u, s, s2; mov.b32 {l, u}, %2; mov.b32 {s, s2}, %3;\n\t"
+        "fma.rn.f32.f16 %0, l, s, 0f80000000; fma.rn.f32.f16 %1, u, s, 0f80000000; }"
+        : "=f"(lo), "=f"(hi) : "r"(h), "r"(sc16x2));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  } else {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));  // exact
+    return r;
+  }
+}
+
 }  // namespace wqmm

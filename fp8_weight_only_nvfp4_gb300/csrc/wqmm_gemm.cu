@@ -37,6 +37,7 @@
 // Every mbarrier wait is bounded; a wait that runs out raises a CTA-wide
 // abort flag, records WQMM_ERR_TIMEOUT, and all roles drain to the TMEM
 // release at the end.
+#include <cstring>
 #include <mutex>
 
 #include "wqmm_device.cuh"
@@ -222,22 +223,14 @@ __device__ __forceinline__ void decode_fp4_word(uint32_t w, uint32_t sc16, uint3
   e2m1x8_to_f16x8(w, h);
   const uint32_t sc2 = __byte_perm(sc16, 0, 0x1010);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t pr;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(pr) : "r"(h[i]), "r"(sc2));  // exact
-    if constexpr (DT == 0) {
-      out[i] = pr;
-    } else {
-      const float2 f = f16x2_to_f32x2(pr);  // exact
-      out[i] = pack2_rn<1>(f.x, f.y);       // exact
-    }
-  }
+  for (int i = 0; i < 4; ++i) out[i] = fold_f16x2<DT>(h[i], sc2);
 }
 
 // KIND 0 = NVFP4 weight, 1 = FP8 weight.  DT 0 = FP16, 1 = BF16.
 template <int DT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmY, int y_tma,
                    const uint8_t* __restrict__ ws, const float* __restrict__ gscale,
                    const float* __restrict__ fscale, const uint16_t* __restrict__ bias,
                    uint16_t* __restrict__ Y, int M, int N, int K, int bs, int* err) {
@@ -263,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&afull[s], kDecWarps * 32);
+      mbar_init(&afull[s], kDecWarps);
     }
     mbar_init(accfull, 1);
     *abort_flag = 0;
@@ -335,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;          // weight row within the tile
     const int n = n0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const int bs_shift = ((bs & (bs - 1)) == 0) ? __ffs(bs) - 1 : -1;
+    const uint8_t* ws_row = ws + (int64_t)n * S;
+    const float* fs_row = fscale + (int64_t)n * S;
     bool ok = true;
     for (int it = 0; it < num_k; ++it) {
       const int s = it % kStages;
@@ -343,10 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sc16 = 0;
       float scf = 0.f;
       if (n < N && kc < K) {
+        const int col = bs_shift >= 0 ? kc >> bs_shift : kc / bs;
         if constexpr (KIND == 0)
-          sc16 = e4m3x2_to_f16x2(__ldg(ws + (int64_t)n * S + kc / bs)) & 0xFFFFu;
+          sc16 = e4m3x2_to_f16x2(__ldg(ws_row + col)) & 0xFFFFu;
         else
-          scf = __ldg(fscale + (int64_t)n * S + kc / bs);
+          scf = __ldg(fs_row + col);
       }
       if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) { ok = false; break; }
       tc_fence_after();
@@ -375,24 +372,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st8(lane_base + kACol + s * (kBK / 2) + 8 * qk, v);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&afull[s]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[s]);  // one arrival per warp
     }
     // Epilogue: this warp's lane quarter, token columns [64 qk, 64 qk + 64).
-    if (ok && wait_bar(accfull, 0, err, abort_flag)) {
+    // With a tensor map for Y the tile is staged transposed, [256 tokens x
+    // 128 n], in the (now idle) activation ring and written by one tensor
+    // store; otherwise each column is stored directly (lanes = consecutive n).
+    const bool have = ok && wait_bar(accfull, 0, err, abort_flag);
+    if (have) {
       tc_fence_after();
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
+      uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + SmemLayout::act);
 #pragma unroll 1
       for (int c0 = 64 * qk; c0 < 64 * qk + 64; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + kAccCol + c0, r);
-        if (n < N) {
+        if (y_tma) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            stage_y[(c0 + j) * kBM + row] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
+        } else if (n < N) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int m = m0 + c0 + j;
             if (m < M) Y[(int64_t)m * N + n] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
           }
         }
+      }
+    }
+    if (y_tma) {
+      // Make the staged tile visible to the tensor-copy engine, then one
+      // elected thread stores it (out-of-range rows and columns are clipped).
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+      if (have && warp == 2 && lane == 0) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                reinterpret_cast<uint64_t>(&tmY)),
+            "r"(n0), "r"(m0), "r"(smem_u32(smem + SmemLayout::act))
+            : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       }
     }
   }
@@ -421,6 +443,15 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
                       KIND == 0 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return kCuda;
+  // Y through a tensor store when its rows are 16-byte multiples.
+  CUtensorMap tmY;
+  int y_tma = 0;
+  std::memset(&tmY, 0, sizeof(tmY));
+  if (a.N % 8 == 0)
+    y_tma = encode_tmap_2d(&tmY, adt, a.Y, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.N * 2, kBM,
+                           kBN, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
+                ? 1
+                : 0;
   static std::once_flag once[2][2];
   std::call_once(once[DT][KIND], [] {
     cudaFuncSetAttribute(gemm_tc_kernel<DT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -428,7 +459,7 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
   });
   dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)((a.M + kBN - 1) / kBN));
   gemm_tc_kernel<DT, KIND><<<grid, kThreads, kSmemBytes, st>>>(
-      tmA, tmW, a.ws, a.gscale, a.fscale, reinterpret_cast<const uint16_t*>(a.bias),
+      tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale, reinterpret_cast<const uint16_t*>(a.bias),
       reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, a.bs, device_error_word());
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }

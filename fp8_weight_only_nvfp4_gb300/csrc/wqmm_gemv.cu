@@ -342,25 +342,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// A decoded f16x2 E2M1 pair times an f16 scale -> 16-bit operand pair (DT).
-// Exact: the products have at most 6 significant bits.
-template <int DT>
-__device__ __forceinline__ uint32_t fold_f16x2(uint32_t h, uint32_t sc16x2) {
-  if constexpr (DT == 1) {
-    float lo, hi;
-    asm("{ .reg .b16 l, u, s, s2; mov.b32 {l, u}, %2; mov.b32 {s, s2}, %3;\n\t"
-        "fma.rn.f32.f16 %0, l, s, 0f80000000; fma.rn.f32.f16 %1, u, s, 0f80000000; }"
-        : "=f"(lo), "=f"(hi) : "r"(h), "r"(sc16x2));
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-  } else {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(sc16x2));  // exact
-    return r;
-  }
-}
-
 // FP8: two E4M3 bytes (low 16 bits) times a float scale -> operand pair,
 // rounded once to the activation type.
 template <int DT>
@@ -687,7 +668,8 @@ int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
 //   activation     [M rows x 256 k]    four 64-k boxes, 128-byte swizzle
 //   block scales   [64 rows x 16 B]    1 KB
 // Four consumer warps, one 16-row MMA tile each, decode and multiply whole
-// steps (both 128-k windows), alternating two accumulator chains.  Waits
+// steps (both 128-k windows), alternating two accumulator chains, and hand a
+// stage back to the producer after the step's last MMA.  Waits
 // block with a suspend-time hint instead of spinning.  A thread-block
 // cluster of C CTAs along gridDim.y splits K; after a cluster barrier every
 // rank writes its partial sums into rank 0's (now idle) stage memory and
@@ -869,8 +851,7 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CU
           x[h][4 * q] = v.x; x[h][4 * q + 1] = v.y; x[h][4 * q + 2] = v.z; x[h][4 * q + 3] = v.w;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);  // operands are in registers now
+      const int st_used = st;
       if (++st == NS) { st = 0; ph ^= 1u; }
       if (i == 0) pdl_launch_dependents();
 #pragma unroll
@@ -896,6 +877,11 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CU
                     x[h][2 * j1 + 1], DT);
         }
       }
+      // Release the stage only once every operand loaded from it has been
+      // consumed: issuing the shared loads and arriving right away let the
+      // next tensor copy overwrite the stage under loads still in flight.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st_used]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc2[i];

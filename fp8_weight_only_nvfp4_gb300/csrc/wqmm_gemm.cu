@@ -12,22 +12,26 @@
 // tensor memory, and never written back to global memory.
 //
 // Tile: 128 weight rows (MMA M) x 256 tokens (MMA N) per CTA, K in stages of
-// 64.  Roles (one CTA = 6 warps):
+// 64.  Roles (one CTA = 10 warps):
 //   warp 0     TMA producer: activation tile [256 tokens x 64 k] (128-byte
 //              swizzle, K-major) and packed weight tile [128 rows x 64 k]
-//              into a 4-stage shared-memory ring;
+//              into a 5-stage shared-memory ring;
 //   warp 1     TMEM owner and MMA issuer (one elected thread):
 //              tcgen05.mma.kind::f16, A = decoded weight from TMEM,
 //              B = activation tile from shared memory, D = FP32 in TMEM;
-//   warps 2-17 decoders: warp w serves TMEM lane quarter (w % 4) and one
-//              quarter (16 k) of each 64-k stage; thread i of the quarter owns
-//              weight row i (TMEM lane i).  It reads its packed bytes from
-//              shared memory, folds the E4M3 block scale (exact for NVFP4:
+//   warps 2-9  decoders: warp w serves TMEM lane quarter (w % 4) and one
+//              half (32 k) of each 64-k stage; thread i of the quarter owns
+//              weight row i (TMEM lane i).  It reads its 16 packed bytes from
+//              shared memory, folds the E4M3 block scales (exact for NVFP4:
 //              <= 6 significant bits, FP4 page §4), writes the 16-bit
-//              operand to TMEM with tcgen05.st, and after the main loop
-//              runs the epilogue for a quarter of the 256 token columns: TMEM ->
-//              registers, * gscale, + bias, one RNE, stores Y[token, n]
-//              (lanes = consecutive n: coalesced).
+//              operands to TMEM with one tcgen05.st, and after the main loop
+//              runs the epilogue for half of the 256 token columns: TMEM ->
+//              registers, * gscale, + bias, one RNE, then Y (through a
+//              shared-memory transpose and one tensor store when the row
+//              pitch allows, else direct stores with lanes = consecutive n).
+//              Two decoder warps per scheduler is the measured optimum: one
+//              leaves the per-stage latency exposed, four spend the issue
+//              slots on per-stage overhead.
 //
 // The weight being the MMA A operand is the FP4 page §4 idea (weight in the
 // A slot, activation in the B slot) carried to tcgen05: the decoded weight
@@ -49,14 +53,15 @@ namespace {
 constexpr int kBM = 128;       // weight rows per tile (MMA M)
 constexpr int kBN = 256;       // tokens per tile (MMA N)
 constexpr int kBK = 64;        // k per stage
-constexpr int kStages = 4;
-constexpr int kDecWarps = 16;  // four per TMEM lane quarter, each a quarter of a stage's k
+constexpr int kStages = 5;
+constexpr int kDecWarps = 8;  // two per TMEM lane quarter, each half of a stage's k
 constexpr int kThreads = (2 + kDecWarps) * 32;
 constexpr int kActStageBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kWStageBytes = kBM * kBK;         // 8 KB (FP8 worst case; NVFP4 uses 4 KB)
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;                      // accumulator: columns [0, 256)
-constexpr int kACol = 256;                      // A stages: columns [256, 256 + 4 * 32)
+constexpr int kACol = 256;                      // A stages: columns [256, 256 + 32 * kStages)
+static_assert(kACol + kStages * (kBK / 2) <= kTmemCols, "TMEM columns");
 
 struct SmemLayout {
   static constexpr int act = 0;
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- decoders, then epilogue ----------------
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int qk = (warp - 2) >> 2;         // which 16-k quarter of each stage
+    const int qk = (warp - 2) >> 2;         // which 32-k half of each stage
     const int row = q * 32 + lane;          // weight row within the tile
     const int n = n0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
@@ -334,48 +339,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = 0; it < num_k; ++it) {
       const int s = it % kStages;
-      // Scale of this 16-k chunk (bs is a multiple of 16).
-      const int kc = it * kBK + 16 * qk;
-      uint32_t sc16 = 0;
-      float scf = 0.f;
-      if (n < N && kc < K) {
-        const int col = bs_shift >= 0 ? kc >> bs_shift : kc / bs;
-        if constexpr (KIND == 0)
-          sc16 = e4m3x2_to_f16x2(__ldg(ws_row + col)) & 0xFFFFu;
-        else
-          scf = __ldg(fs_row + col);
+      // Scales of this warp's two 16-k chunks (bs is a multiple of 16).
+      const int kc = it * kBK + 32 * qk;
+      uint32_t sca = 0, scb = 0;
+      float sfa = 0.f, sfb = 0.f;
+      if (n < N) {
+        const int ca = bs_shift >= 0 ? kc >> bs_shift : kc / bs;
+        const int cb = bs_shift >= 0 ? (kc + 16) >> bs_shift : (kc + 16) / bs;
+        if constexpr (KIND == 0) {
+          if (kc < K) sca = e4m3x2_to_f16x2(__ldg(ws_row + ca)) & 0xFFFFu;
+          if (kc + 16 < K) scb = e4m3x2_to_f16x2(__ldg(ws_row + cb)) & 0xFFFFu;
+        } else {
+          if (kc < K) sfa = __ldg(fs_row + ca);
+          if (kc + 16 < K) sfb = __ldg(fs_row + cb);
+        }
       }
       if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint8_t* wt = smem + SmemLayout::w + s * kWStageBytes;
-      uint32_t v[8];
+      uint32_t v[16];
       if constexpr (KIND == 0) {
-        // 8 bytes (16 k) of this row's 32-byte stage run, 32-byte swizzle.
-        const uint32_t off = row * 32 + 8 * qk;
+        // 16 bytes (32 k) of this row's 32-byte stage run, 32-byte swizzle.
+        const uint32_t off = row * 32 + 16 * qk;
         const uint32_t phys = off ^ (((off >> 7) & 1u) << 4);
-        const uint2 pw = *reinterpret_cast<const uint2*>(wt + phys);
-        decode_fp4_word<DT>(pw.x, sc16, &v[0]);
-        decode_fp4_word<DT>(pw.y, sc16, &v[4]);
+        const uint4 pw = *reinterpret_cast<const uint4*>(wt + phys);
+        decode_fp4_word<DT>(pw.x, sca, &v[0]);
+        decode_fp4_word<DT>(pw.y, sca, &v[4]);
+        decode_fp4_word<DT>(pw.z, scb, &v[8]);
+        decode_fp4_word<DT>(pw.w, scb, &v[12]);
       } else {
-        // 16 bytes (16 k) of this row's 64-byte stage run, 64-byte swizzle.
-        const uint4 p = lds_swz<3>(wt, row * 64 + 16 * qk);
-        const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+        // 32 bytes (32 k) of this row's 64-byte stage run, 64-byte swizzle.
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int c = 0; c < 2; ++c) {
+          const uint4 p = lds_swz<3>(wt, row * 64 + 32 * qk + 16 * c);
+          const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+          const float scf = c ? sfb : sfa;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float2 e = f16x2_to_f32x2(e4m3x2_to_f16x2((w4[i] >> (16 * h)) & 0xFFFFu));
-            v[2 * i + h] = pack2_rn<DT>(e.x * scf, e.y * scf);
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float2 e = f16x2_to_f32x2(e4m3x2_to_f16x2((w4[i] >> (16 * h)) & 0xFFFFu));
+              v[8 * c + 2 * i + h] = pack2_rn<DT>(e.x * scf, e.y * scf);
+            }
           }
         }
       }
-      tmem_st8(lane_base + kACol + s * (kBK / 2) + 8 * qk, v);
+      tmem_st16(lane_base + kACol + s * (kBK / 2) + 16 * qk, v);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[s]);  // one arrival per warp
     }
-    // Epilogue: this warp's lane quarter, token columns [64 qk, 64 qk + 64).
+    // Epilogue: this warp's lane quarter, token columns [128 qk, 128 qk + 128).
     // With a tensor map for Y the tile is staged transposed, [256 tokens x
     // 128 n], in the (now idle) activation ring and written by one tensor
     // store; otherwise each column is stored directly (lanes = consecutive n).
@@ -386,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
       uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + SmemLayout::act);
 #pragma unroll 1
-      for (int c0 = 64 * qk; c0 < 64 * qk + 64; c0 += 32) {
+      for (int c0 = 128 * qk; c0 < 128 * qk + 128; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + kAccCol + c0, r);
         if (y_tma) {

@@ -12,26 +12,27 @@
 // tensor memory, and never written back to global memory.
 //
 // Tile: 128 weight rows (MMA M) x 256 tokens (MMA N) per CTA, K in stages of
-// 64.  Roles (one CTA = 10 warps):
+// 64.  Roles (one CTA = 18 warps):
 //   warp 0     TMA producer: activation tile [256 tokens x 64 k] (128-byte
 //              swizzle, K-major) and packed weight tile [128 rows x 64 k]
-//              into a 5-stage shared-memory ring;
+//              into a shared-memory ring (6 stages for NVFP4, 5 for FP8);
 //   warp 1     TMEM owner and MMA issuer (one elected thread):
 //              tcgen05.mma.kind::f16, A = decoded weight from TMEM,
 //              B = activation tile from shared memory, D = FP32 in TMEM;
-//   warps 2-9  decoders: warp w serves TMEM lane quarter (w % 4) and one
-//              half (32 k) of each 64-k stage; thread i of the quarter owns
-//              weight row i (TMEM lane i).  It reads its 16 packed bytes from
+//   warps 2-17 decoders: warp w serves TMEM lane quarter (w % 4) and decodes
+//              every fourth stage in full; thread i of the quarter owns
+//              weight row i (TMEM lane i).  It reads its packed bytes from
 //              shared memory, folds the E4M3 block scales (exact for NVFP4:
 //              <= 6 significant bits, FP4 page §4), writes the 16-bit
 //              operands to TMEM with one tcgen05.st, and after the main loop
-//              runs the epilogue for half of the 256 token columns: TMEM ->
-//              registers, * gscale, + bias, one RNE, then Y (through a
+//              runs the epilogue for a quarter of the 256 token columns: TMEM
+//              -> registers, * gscale, + bias, one RNE, then Y (through a
 //              shared-memory transpose and one tensor store when the row
 //              pitch allows, else direct stores with lanes = consecutive n).
-//              Two decoder warps per scheduler is the measured optimum: one
-//              leaves the per-stage latency exposed, four spend the issue
-//              slots on per-stage overhead.
+//              Measured: without the tensor-memory stores the kernel runs at
+//              the speed of the plain MMA pipeline; the stores complete late
+//              while the MMA streams, so the four warps of a quarter keep
+//              four stages in flight instead of splitting one stage's k.
 //
 // The weight being the MMA A operand is the FP4 page §4 idea (weight in the
 // A slot, activation in the B slot) carried to tcgen05: the decoded weight
@@ -53,29 +54,34 @@ namespace {
 constexpr int kBM = 128;       // weight rows per tile (MMA M)
 constexpr int kBN = 256;       // tokens per tile (MMA N)
 constexpr int kBK = 64;        // k per stage
-constexpr int kStages = 5;
-constexpr int kDecWarps = 8;  // two per TMEM lane quarter, each half of a stage's k
+constexpr int kDecWarps = 16;  // four per TMEM lane quarter, taking the stages in turn
 constexpr int kThreads = (2 + kDecWarps) * 32;
 constexpr int kActStageBytes = kBN * kBK * 2;   // 32 KB
-constexpr int kWStageBytes = kBM * kBK;         // 8 KB (FP8 worst case; NVFP4 uses 4 KB)
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;                      // accumulator: columns [0, 256)
-constexpr int kACol = 256;                      // A stages: columns [256, 256 + 32 * kStages)
-static_assert(kACol + kStages * (kBK / 2) <= kTmemCols, "TMEM columns");
+constexpr int kACol = 256;                      // A stages: columns [256, 256 + 32 * stages)
 
-struct SmemLayout {
+// Ring depth per weight format: as many stages as shared memory holds (the
+// ring has to cover the tensor-copy latency; a stage is 32 KB of activation
+// plus the packed weight tile, 4 KB for NVFP4 and 8 KB for FP8).
+template <int KIND>
+struct GemmCfg {
+  static constexpr int stages = KIND == 0 ? 6 : 5;
+  static constexpr int wstage = KIND == 0 ? kBM * kBK / 2 : kBM * kBK;
   static constexpr int act = 0;
-  static constexpr int w = act + kStages * kActStageBytes;
-  static constexpr int bars = w + kStages * kWStageBytes;
+  static constexpr int w = act + stages * kActStageBytes;
+  static constexpr int bars = w + stages * wstage;
   static constexpr int full = bars;
-  static constexpr int empty = full + 8 * kStages;
-  static constexpr int afull = empty + 8 * kStages;
-  static constexpr int accfull = afull + 8 * kStages;
+  static constexpr int empty = full + 8 * stages;
+  static constexpr int afull = empty + 8 * stages;
+  static constexpr int accfull = afull + 8 * stages;
   static constexpr int tmem_slot = accfull + 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int total = abort_flag + 4;
+  static constexpr int smem_bytes = total + 1024;  // + alignment slack
+  static_assert(kACol + stages * (kBK / 2) <= kTmemCols, "TMEM columns");
+  static_assert(smem_bytes <= 227 * 1024, "shared memory");
 };
-constexpr int kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
 // ---------------------------------------------------------------------------
 // tcgen05 wrappers
@@ -239,15 +245,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const uint8_t* __restrict__ ws, const float* __restrict__ gscale,
                    const float* __restrict__ fscale, const uint16_t* __restrict__ bias,
                    uint16_t* __restrict__ Y, int M, int N, int K, int bs, int* err) {
+  using L = GemmCfg<KIND>;
+  constexpr int kStages = L::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SmemLayout::full);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + SmemLayout::empty);
-  uint64_t* afull = reinterpret_cast<uint64_t*>(smem + SmemLayout::afull);
-  uint64_t* accfull = reinterpret_cast<uint64_t*>(smem + SmemLayout::accfull);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::tmem_slot);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::abort_flag);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L::empty);
+  uint64_t* afull = reinterpret_cast<uint64_t*>(smem + L::afull);
+  uint64_t* accfull = reinterpret_cast<uint64_t*>(smem + L::accfull);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort_flag);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -261,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&afull[s], kDecWarps);
+      mbar_init(&afull[s], 4);  // one decoder warp per lane quarter
     }
     mbar_init(accfull, 1);
     *abort_flag = 0;
@@ -286,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % kStages;
         if (it >= kStages && !wait_bar(&empty[s], ((it / kStages) + 1) & 1, err, abort_flag)) break;
         mbar_arrive_expect_tx(&full[s], bytes);
-        tma_load_2d(smem + SmemLayout::act + s * kActStageBytes, &tmA, it * kBK, m0, &full[s]);
-        tma_load_2d(smem + SmemLayout::w + s * kWStageBytes, &tmW, it * kWBytes, n0, &full[s]);
+        tma_load_2d(smem + L::act + s * kActStageBytes, &tmA, it * kBK, m0, &full[s]);
+        tma_load_2d(smem + L::w + s * L::wstage, &tmW, it * kWBytes, n0, &full[s]);
         ++issued;
       }
       // No copy may still be landing in shared memory when the CTA exits:
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_bar(&full[s], par, err, abort_flag) && wait_bar(&afull[s], par, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t act_addr = smem_u32(smem + SmemLayout::act + s * kActStageBytes);
+        const uint32_t act_addr = smem_u32(smem + L::act + s * kActStageBytes);
         const uint64_t bdesc = desc_kmajor_sw128(act_addr);
 #pragma unroll
         for (int j = 0; j < kBK / 16; ++j) {
@@ -328,52 +336,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- decoders, then epilogue ----------------
+    // Warp w serves TMEM lane quarter q = w % 4 and decodes every fourth
+    // stage (phase j = (w - 2) / 4) in full: the four warps of a quarter
+    // have four stages in flight, so the latency of one warp's stage
+    // (shared load, decode, tensor-memory store, which completes late while
+    // the MMA streams) is spread over four stages.
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int qk = (warp - 2) >> 2;         // which 32-k half of each stage
+    const int j4 = (warp - 2) >> 2;         // stage phase of this warp
     const int row = q * 32 + lane;          // weight row within the tile
     const int n = n0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const int bs_shift = ((bs & (bs - 1)) == 0) ? __ffs(bs) - 1 : -1;
     const uint8_t* ws_row = ws + (int64_t)n * S;
     const float* fs_row = fscale + (int64_t)n * S;
-    bool ok = true;
-    for (int it = 0; it < num_k; ++it) {
-      const int s = it % kStages;
-      // Scales of this warp's two 16-k chunks (bs is a multiple of 16).
-      const int kc = it * kBK + 32 * qk;
-      uint32_t sca = 0, scb = 0;
-      float sfa = 0.f, sfb = 0.f;
-      if (n < N) {
-        const int ca = bs_shift >= 0 ? kc >> bs_shift : kc / bs;
-        const int cb = bs_shift >= 0 ? (kc + 16) >> bs_shift : (kc + 16) / bs;
-        if constexpr (KIND == 0) {
-          if (kc < K) sca = e4m3x2_to_f16x2(__ldg(ws_row + ca)) & 0xFFFFu;
-          if (kc + 16 < K) scb = e4m3x2_to_f16x2(__ldg(ws_row + cb)) & 0xFFFFu;
-        } else {
-          if (kc < K) sfa = __ldg(fs_row + ca);
-          if (kc + 16 < K) sfb = __ldg(fs_row + cb);
+    // Raw scales of the four 16-k chunks of stage `it` (bs is a multiple of
+    // 16), fetched one turn (four stages) ahead of their use.
+    auto fetch = [&](int it, uint32_t (&r)[4]) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int k1 = it * kBK + 16 * c;
+        r[c] = 0u;
+        if (n < N && it < num_k && k1 < K) {
+          const int col = bs_shift >= 0 ? k1 >> bs_shift : k1 / bs;
+          if constexpr (KIND == 0)
+            r[c] = __ldg(ws_row + col);
+          else
+            r[c] = __float_as_uint(__ldg(fs_row + col));
         }
       }
-      if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const uint8_t* wt = smem + SmemLayout::w + s * kWStageBytes;
-      uint32_t v[16];
-      if constexpr (KIND == 0) {
-        // 16 bytes (32 k) of this row's 32-byte stage run, 32-byte swizzle.
-        const uint32_t off = row * 32 + 16 * qk;
-        const uint32_t phys = off ^ (((off >> 7) & 1u) << 4);
-        const uint4 pw = *reinterpret_cast<const uint4*>(wt + phys);
-        decode_fp4_word<DT>(pw.x, sca, &v[0]);
-        decode_fp4_word<DT>(pw.y, sca, &v[4]);
-        decode_fp4_word<DT>(pw.z, scb, &v[8]);
-        decode_fp4_word<DT>(pw.w, scb, &v[12]);
-      } else {
-        // 32 bytes (32 k) of this row's 64-byte stage run, 64-byte swizzle.
+    };
+    uint32_t scn[4];
+    fetch(j4, scn);
+    bool ok = true;
+    for (int it = j4; it < num_k; it += 4) {
+      const int s = it % kStages;
+      uint32_t sc[4];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint4 p = lds_swz<3>(wt, row * 64 + 32 * qk + 16 * c);
+      for (int c = 0; c < 4; ++c) sc[c] = scn[c];
+      fetch(it + 4, scn);
+      if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint8_t* wt = smem + L::w + s * L::wstage;
+      uint32_t v[32];
+      if constexpr (KIND == 0) {
+        // The row's 32-byte stage run (64 k), 32-byte swizzle.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t off = row * 32 + 16 * h;
+          const uint32_t phys = off ^ (((off >> 7) & 1u) << 4);
+          const uint4 pw = *reinterpret_cast<const uint4*>(wt + phys);
+          const uint32_t sa = e4m3x2_to_f16x2(sc[2 * h]) & 0xFFFFu;
+          const uint32_t sb = e4m3x2_to_f16x2(sc[2 * h + 1]) & 0xFFFFu;
+          decode_fp4_word<DT>(pw.x, sa, &v[16 * h + 0]);
+          decode_fp4_word<DT>(pw.y, sa, &v[16 * h + 4]);
+          decode_fp4_word<DT>(pw.z, sb, &v[16 * h + 8]);
+          decode_fp4_word<DT>(pw.w, sb, &v[16 * h + 12]);
+        }
+      } else {
+        // The row's 64-byte stage run (64 k), 64-byte swizzle.
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 p = lds_swz<3>(wt, row * 64 + 16 * c);
           const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
-          const float scf = c ? sfb : sfa;
+          const float scf = __uint_as_float(sc[c]);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -384,13 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tmem_st16(lane_base + kACol + s * (kBK / 2) + 16 * qk, v);
+      tmem_st32(lane_base + kACol + s * (kBK / 2), v);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[s]);  // one arrival per warp
+      if (lane == 0) mbar_arrive(&afull[s]);  // one arrival per lane quarter
     }
-    // Epilogue: this warp's lane quarter, token columns [128 qk, 128 qk + 128).
+    // Epilogue: this warp's lane quarter, token columns [64 j4, 64 j4 + 64).
     // With a tensor map for Y the tile is staged transposed, [256 tokens x
     // 128 n], in the (now idle) activation ring and written by one tensor
     // store; otherwise each column is stored directly (lanes = consecutive n).
@@ -399,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
-      uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + SmemLayout::act);
+      uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + L::act);
 #pragma unroll 1
-      for (int c0 = 128 * qk; c0 < 128 * qk + 128; c0 += 32) {
+      for (int c0 = 64 * j4; c0 < 64 * j4 + 64; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + kAccCol + c0, r);
         if (y_tma) {
@@ -426,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile(
             "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                 reinterpret_cast<uint64_t>(&tmY)),
-            "r"(n0), "r"(m0), "r"(smem_u32(smem + SmemLayout::act))
+            "r"(n0), "r"(m0), "r"(smem_u32(smem + L::act))
             : "memory");
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -470,10 +498,10 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
   static std::once_flag once[2][2];
   std::call_once(once[DT][KIND], [] {
     cudaFuncSetAttribute(gemm_tc_kernel<DT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSmemBytes);
+                         GemmCfg<KIND>::smem_bytes);
   });
   dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)((a.M + kBN - 1) / kBN));
-  gemm_tc_kernel<DT, KIND><<<grid, kThreads, kSmemBytes, st>>>(
+  gemm_tc_kernel<DT, KIND><<<grid, kThreads, GemmCfg<KIND>::smem_bytes, st>>>(
       tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale, reinterpret_cast<const uint16_t*>(a.bias),
       reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, a.bs, device_error_word());
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
@@ -484,7 +512,8 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
 bool gemm_supports(const GemvArgs& a) {
   const DeviceInfo& d = device_info();
   if (d.cc_major != 10) return false;
-  if (d.max_smem_optin < kSmemBytes) return false;
+  if (d.max_smem_optin < (a.kind == 0 ? GemmCfg<0>::smem_bytes : GemmCfg<1>::smem_bytes))
+    return false;
   if (a.M <= 8 || a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31)) return false;
   if (a.bs % 16 != 0) return false;
   if (a.kind == 0) return a.K % 32 == 0;   // packed row stride must be a multiple of 16 bytes

@@ -734,7 +734,7 @@ __device__ __forceinline__ bool wait_abortable(uint64_t* bar, uint32_t parity, i
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CUtensorMap tmW,
+__global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__ CUtensorMap tmW,
                                                       const __grid_constant__ CUtensorMap tmS,
                                                       const __grid_constant__ CUtensorMap tmA,
                                                       const TmaGemvParams p) {
@@ -778,20 +778,32 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma(const __grid_constant__ CU
     // an earlier kernel in the stream still runs).  Only the first ring's
     // worth: prefetching a long K-range ahead would evict itself from L2.
     if (lane == 0) {
-      const int npf = min(nst, NS + 2);
-      for (int i = 0; i < npf; ++i) {
+      // The weight and its scales do not depend on the previous kernel: the
+      // first ring's worth of them is copied into shared memory before the
+      // dependency wait, and the next two steps are pulled into L2.  Only
+      // the activation copies wait.
+      const int npre = min(nst, NS);
+      for (int i = 0; i < npre; ++i) {
+        uint8_t* base = sm + L.stages + i * kTStage;
+        mbar_arrive_expect_tx(&full[i], kTStepW + kTStepS + a_bytes);
+        tma_load_2d(base, &tmW, (s_lo + i) * 128, row_base, &full[i]);
+        tma_load_2d(base + kTStepW + kTStepA, &tmS, (s_lo + i) * 16, row_base, &full[i]);
+      }
+      for (int i = npre; i < min(nst, NS + 2); ++i) {
         tma_prefetch_2d(&tmW, (s_lo + i) * 128, row_base);
         tma_prefetch_2d(&tmS, (s_lo + i) * 16, row_base);
       }
-    }
-    if (lane == 0) {
-      prefetch_tmap(&tmW);
-      prefetch_tmap(&tmS);
       prefetch_tmap(&tmA);
       pdl_wait();
-      int issued = 0, st = 0;
-      uint32_t ph = 0;
-      for (int i = 0; i < nst; ++i) {
+      for (int i = 0; i < npre; ++i) {
+        uint8_t* base = sm + L.stages + i * kTStage;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          tma_load_2d(base + kTStepW + b * 1024, &tmA, (s_lo + i) * 256 + 64 * b, 0, &full[i]);
+      }
+      int issued = npre, st = npre % NS;
+      uint32_t ph = npre == NS ? 1u : 0u;
+      for (int i = npre; i < nst; ++i) {
         if (i >= NS && !wait_abortable(&empty[st], ph ^ 1u, p.err, abort_flag)) break;
         uint8_t* base = sm + L.stages + st * kTStage;
         mbar_arrive_expect_tx(&full[st], kTStepW + kTStepS + a_bytes);

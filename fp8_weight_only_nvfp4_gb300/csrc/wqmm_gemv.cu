@@ -771,6 +771,18 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 
+  // Epilogue constants (global scale, bias) do not depend on the previous
+  // kernel: fetched now, off the critical path at the end.
+  const int ep_row0 = row_base + (warp < kTCons ? warp : 0) * 16 + g;
+  float ep_gs = 0.f, ep_b0 = 0.f, ep_b1 = 0.f;
+  if (warp < kTCons && rank == 0) {
+    ep_gs = __ldg(p.gscale);
+    if (p.bias != nullptr) {
+      if (ep_row0 < p.N) ep_b0 = act_to_f32<DT>(__ldg(p.bias + ep_row0));
+      if (ep_row0 + 8 < p.N) ep_b1 = act_to_f32<DT>(__ldg(p.bias + ep_row0 + 8));
+    }
+  }
+
   if (warp == kTCons) {
     // ---------------- producer ----------------
     // Before the dependency wait: pull the first stages' weight and scale
@@ -921,18 +933,12 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
   } else if (!owner) {
     return;
   }
-  const int row0 = row_base + warp * 16 + g;
-  const int row1 = row0 + 8;
-  const float gs = __ldg(p.gscale);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int n = (i < 2) ? row0 : row1;
+    const int n = (i < 2) ? ep_row0 : ep_row0 + 8;
     const int m = 2 * t + (i & 1);
-    if (n < p.N && m < p.M) {
-      float y = acc[i] * gs;
-      if (p.bias) y += act_to_f32<DT>(__ldg(p.bias + n));
-      p.Y[(int64_t)m * p.N + n] = to_act_rn<DT>(y);
-    }
+    if (n < p.N && m < p.M)
+      p.Y[(int64_t)m * p.N + n] = to_act_rn<DT>(acc[i] * ep_gs + ((i < 2) ? ep_b0 : ep_b1));
   }
 }
 

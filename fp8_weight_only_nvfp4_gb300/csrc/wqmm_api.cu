@@ -9,6 +9,7 @@
 //   empty output          -> return, no launch
 //   K == 0                -> Y = bias (or 0)
 //   M <= 8                -> decode GEMV
+//   M <= 32, NVFP4 bs 16, K % 256 == 0 -> decode GEMV (up to four 8-row tiles)
 //   M > 8, GEMM-eligible  -> fused tcgen05 GEMM (weight decoded in the main loop)
 //   otherwise             -> decode GEMV, one launch per 8-row group
 #include <mutex>
@@ -118,6 +119,10 @@ int check_common(int64_t M, int64_t N, int64_t K, int bs, int dtype) {
 int matmul_common(GemvArgs& a, cudaStream_t st) {
   if (a.K == 0) return launch_fill_bias(a.bias, a.Y, a.M, a.N, a.dtype, st);
   if (a.M <= 8) return launch_gemv(a, st);
+  // Up to 32 rows the decode GEMV shares each decoded weight across all of
+  // them and stays bound by the weight stream; the 256-token GEMM tile would
+  // leave most of the GPU idle at these sizes.
+  if (a.M <= 32 && gemv_tma_supports(a)) return launch_gemv(a, st);
   if (gemm_supports(a)) return launch_gemm(a, st);
   // Decode GEMV per group of rows (blockIdx.z covers up to 65535 groups).
   const int64_t rows_per_launch = int64_t(8) * 65535;

@@ -659,7 +659,8 @@ int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
 
 
 // ===========================================================================
-// TMA-fed decode GEMV for NVFP4 with block_size 16 and K % 256 == 0.
+// TMA-fed decode GEMV for NVFP4 with block_size 16 and K % 256 == 0,
+// M <= 32 (NT = ceil(M / 8) activation tiles of the MMA's 8 columns).
 //
 // Same MMA mapping as gemv_fast, with the bytes in flight held in shared
 // memory instead of registers.  A producer warp streams, per 256-k step,
@@ -668,23 +669,33 @@ int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
 //   activation     [M rows x 256 k]    four 64-k boxes, 128-byte swizzle
 //   block scales   [64 rows x 16 B]    1 KB
 // Four consumer warps, one 16-row MMA tile each, decode and multiply whole
-// steps (both 128-k windows), alternating two accumulator chains, and hand a
-// stage back to the producer after the step's last MMA.  Waits
-// block with a suspend-time hint instead of spinning.  A thread-block
-// cluster of C CTAs along gridDim.y splits K; after a cluster barrier every
-// rank writes its partial sums into rank 0's (now idle) stage memory and
-// rank 0 adds them in rank order: deterministic, no global scratch.
+// steps (both 128-k windows), alternating two accumulator chains per
+// activation tile: each decoded weight fragment feeds the MMAs of all NT
+// activation tiles.  A stage goes back to the producer after the step's
+// last MMA.  Waits block with a suspend-time hint instead of spinning.  A
+// thread-block cluster of C CTAs along gridDim.y splits K; after a cluster
+// barrier every rank writes its partial sums into rank 0's (now idle) stage
+// memory and rank 0 adds them in rank order: deterministic, no global
+// scratch.
 // ===========================================================================
 
 constexpr int kTTiles = 4;                  // 16-row tiles (= consumer warps) per CTA
 constexpr int kTRows = 16 * kTTiles;        // 64 weight rows per CTA
 constexpr int kTCons = kTTiles;             // consumer warps
 constexpr int kTStepW = kTRows * 128;       // packed bytes per step
-constexpr int kTStepA = 4 * 1024;           // activation boxes (1024-aligned each)
 constexpr int kTStepS = kTRows * 16;        // scale bytes per step
-constexpr int kTStage = kTStepW + kTStepA + kTStepS;  // 13 KB
 constexpr int kTMaxStages = 8;
 constexpr int kTThreads = (kTCons + 1) * 32;
+constexpr int kTMaxM = 32;
+
+// Per activation-tile count NT: each 64-k activation box (M <= 8 NT rows of
+// 128 bytes) sits in its own 1024-aligned slot of NT KB.
+template <int NT>
+struct TStage {
+  static constexpr int slot = 1024 * NT;
+  static constexpr int stepA = 4 * slot;
+  static constexpr int bytes = kTStepW + stepA + kTStepS;
+};
 
 struct TmaGemvParams {
   const float* gscale;
@@ -698,9 +709,9 @@ struct TmaGemvParams {
 
 struct TmaGemvSmem {
   int stages, bars, total;
-  __host__ __device__ TmaGemvSmem(int nstages) {
+  __host__ __device__ TmaGemvSmem(int nstages, int stage_bytes) {
     stages = 0;
-    bars = stages + nstages * kTStage;
+    bars = stages + nstages * stage_bytes;
     total = bars + 2 * kTMaxStages * 8 + 16;
   }
 };
@@ -733,8 +744,8 @@ __device__ __forceinline__ bool wait_abortable(uint64_t* bar, uint32_t parity, i
   return false;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__ CUtensorMap tmW,
+template <int DT, int NT>
+__global__ void __launch_bounds__(kTThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gemv_tma(const __grid_constant__ CUtensorMap tmW,
                                                       const __grid_constant__ CUtensorMap tmS,
                                                       const __grid_constant__ CUtensorMap tmA,
                                                       const TmaGemvParams p) {
@@ -743,7 +754,8 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
                                            ~uintptr_t(1023));
   const int C = gridDim.y;
   const int rank = blockIdx.y;
-  const TmaGemvSmem L(p.nstages);
+  constexpr int kTStage = TStage<NT>::bytes, kTStepA = TStage<NT>::stepA, kSlot = TStage<NT>::slot;
+  const TmaGemvSmem L(p.nstages, kTStage);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + kTMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kTMaxStages);
@@ -769,7 +781,11 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
   if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   __syncthreads();
 
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
 
   // Epilogue constants (global scale, bias) do not depend on the previous
   // kernel: fetched now, off the critical path at the end.
@@ -785,10 +801,6 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
 
   if (warp == kTCons) {
     // ---------------- producer ----------------
-    // Before the dependency wait: pull the first stages' weight and scale
-    // tiles into L2 (prefetches return no data, so they are safe even while
-    // an earlier kernel in the stream still runs).  Only the first ring's
-    // worth: prefetching a long K-range ahead would evict itself from L2.
     if (lane == 0) {
       // The weight and its scales do not depend on the previous kernel: the
       // first ring's worth of them is copied into shared memory before the
@@ -811,7 +823,7 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
         uint8_t* base = sm + L.stages + i * kTStage;
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          tma_load_2d(base + kTStepW + b * 1024, &tmA, (s_lo + i) * 256 + 64 * b, 0, &full[i]);
+          tma_load_2d(base + kTStepW + b * kSlot, &tmA, (s_lo + i) * 256 + 64 * b, 0, &full[i]);
       }
       int issued = npre, st = npre % NS;
       uint32_t ph = npre == NS ? 1u : 0u;
@@ -822,7 +834,7 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
         tma_load_2d(base, &tmW, (s_lo + i) * 128, row_base, &full[st]);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          tma_load_2d(base + kTStepW + b * 1024, &tmA, (s_lo + i) * 256 + 64 * b, 0, &full[st]);
+          tma_load_2d(base + kTStepW + b * kSlot, &tmA, (s_lo + i) * 256 + 64 * b, 0, &full[st]);
         tma_load_2d(base + kTStepW + kTStepA, &tmS, (s_lo + i) * 16, row_base, &full[st]);
         ++issued;
         if (++st == NS) { st = 0; ph ^= 1u; }
@@ -841,7 +853,15 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
     // outputs m >= M, which are never stored.
     const int tile = warp;
     const int r0 = tile * 16 + g, r1 = r0 + 8;  // rows within the CTA
-    const int ga = g < p.M ? g : g % p.M;
+    // Activation row of tile j for this lane: 8 j + g, or a valid row when
+    // that is past M (its MMA column only feeds outputs that are not stored).
+    uint32_t a_row[NT], a_sw[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int r = 8 * j + g < p.M ? 8 * j + g : (8 * j + g) % p.M;
+      a_row[j] = (uint32_t)r * 128u;
+      a_sw[j] = (uint32_t)(r & 7);
+    }
     uint32_t w_off[2][2], s_off[2][2], a_off[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -849,11 +869,14 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
       w_off[h][1] = (r1 * 128 + 64 * h + 16 * t) ^ ((r1 & 7) << 4);
       s_off[h][0] = kTStepW + kTStepA + r0 * 16 + 8 * h + 2 * t;
       s_off[h][1] = kTStepW + kTStepA + r1 * 16 + 8 * h + 2 * t;
-      a_off[h] = kTStepW + (2 * h + (t >> 1)) * 1024 + ga * 128;
+      a_off[h] = kTStepW + (2 * h + (t >> 1)) * kSlot;
     }
     const uint32_t a_c0 = 4 * (t & 1);
-    const uint32_t a_sw = (uint32_t)(ga & 7);
-    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc2[j][i] = 0.f;
     int st = 0;
     uint32_t ph = 0;
     for (int i = 0; i < nst; ++i) {
@@ -861,7 +884,7 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
       const uint8_t* stage = sm + L.stages + st * kTStage;
       uint4 pw[2][2];
       uint32_t sb[2][2];
-      uint32_t x[2][16];
+      uint32_t x[2][16];   // activation tile 0 (NT == 1: all of it)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         pw[h][0] = *reinterpret_cast<const uint4*>(stage + w_off[h][0]);
@@ -870,8 +893,8 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
         sb[h][1] = *reinterpret_cast<const uint16_t*>(stage + s_off[h][1]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 v =
-              *reinterpret_cast<const uint4*>(stage + a_off[h] + (((a_c0 + q) ^ a_sw) << 4));
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + a_off[h] + a_row[0] +
+                                                          (((a_c0 + q) ^ a_sw[0]) << 4));
           x[h][4 * q] = v.x; x[h][4 * q + 1] = v.y; x[h][4 * q + 2] = v.z; x[h][4 * q + 3] = v.w;
         }
       }
@@ -893,12 +916,20 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
           e2m1x8_to_f16x8(p1[q], e1);
           const uint32_t s0 = sc0[q >> 1], s1 = sc1[q >> 1];
           const int j0 = 2 * q, j1 = 2 * q + 1;
-          mma_16816(acc, fold_f16x2<DT>(e0[0], s0), fold_f16x2<DT>(e1[0], s1),
-                    fold_f16x2<DT>(e0[1], s0), fold_f16x2<DT>(e1[1], s1), x[h][2 * j0],
-                    x[h][2 * j0 + 1], DT);
-          mma_16816(acc2, fold_f16x2<DT>(e0[2], s0), fold_f16x2<DT>(e1[2], s1),
-                    fold_f16x2<DT>(e0[3], s0), fold_f16x2<DT>(e1[3], s1), x[h][2 * j1],
-                    x[h][2 * j1 + 1], DT);
+          const uint32_t fa0 = fold_f16x2<DT>(e0[0], s0), fa1 = fold_f16x2<DT>(e1[0], s1);
+          const uint32_t fa2 = fold_f16x2<DT>(e0[1], s0), fa3 = fold_f16x2<DT>(e1[1], s1);
+          const uint32_t fb0 = fold_f16x2<DT>(e0[2], s0), fb1 = fold_f16x2<DT>(e1[2], s1);
+          const uint32_t fb2 = fold_f16x2<DT>(e0[3], s0), fb3 = fold_f16x2<DT>(e1[3], s1);
+          mma_16816(acc[0], fa0, fa1, fa2, fa3, x[h][2 * j0], x[h][2 * j0 + 1], DT);
+          mma_16816(acc2[0], fb0, fb1, fb2, fb3, x[h][2 * j1], x[h][2 * j1 + 1], DT);
+#pragma unroll
+          for (int j = 1; j < NT; ++j) {
+            // The same decoded fragment against activation tile j.
+            const uint4 v = *reinterpret_cast<const uint4*>(stage + a_off[h] + a_row[j] +
+                                                            (((a_c0 + q) ^ a_sw[j]) << 4));
+            mma_16816(acc[j], fa0, fa1, fa2, fa3, v.x, v.y, DT);
+            mma_16816(acc2[j], fb0, fb1, fb2, fb3, v.z, v.w, DT);
+          }
         }
       }
       // Release the stage only once every operand loaded from it has been
@@ -908,7 +939,9 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
       if (lane == 0) mbar_arrive(&empty[st_used]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[j][i] += acc2[j][i];
   }
 
   // Cross-CTA reduction (rank order) into rank 0's idle stage memory.
@@ -919,43 +952,63 @@ __global__ void __launch_bounds__(kTThreads, 4) gemv_tma(const __grid_constant__
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // peers are running
     cluster_sync();                                              // every ring is drained
     if (owner) {
-      const uint32_t local = smem_u32(red + (rank * kTCons + warp) * 32 + lane);
-      st_cluster_f32x4(mapa_shared(local, 0), acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const uint32_t local = smem_u32(red + ((rank * kTCons + warp) * NT + j) * 32 + lane);
+        st_cluster_f32x4(mapa_shared(local, 0), acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+      }
     }
     cluster_sync();
     if (rank != 0 || !owner) return;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-    for (int r = 0; r < C; ++r) {
-      const float4 v = red[(r * kTCons + warp) * 32 + lane];
-      acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
+      for (int r = 0; r < C; ++r) {
+        const float4 v = red[((r * kTCons + warp) * NT + j) * 32 + lane];
+        acc[j][0] += v.x; acc[j][1] += v.y; acc[j][2] += v.z; acc[j][3] += v.w;
+      }
     }
   } else if (!owner) {
     return;
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int n = (i < 2) ? ep_row0 : ep_row0 + 8;
-    const int m = 2 * t + (i & 1);
-    if (n < p.N && m < p.M)
-      p.Y[(int64_t)m * p.N + n] = to_act_rn<DT>(acc[i] * ep_gs + ((i < 2) ? ep_b0 : ep_b1));
-  }
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int n = (i < 2) ? ep_row0 : ep_row0 + 8;
+      const int m = 8 * j + 2 * t + (i & 1);
+      if (n < p.N && m < p.M)
+        p.Y[(int64_t)m * p.N + n] = to_act_rn<DT>(acc[j][i] * ep_gs + ((i < 2) ? ep_b0 : ep_b1));
+    }
 }
 
 struct TmaPlan {
-  int C = 1, spc = 1, nstages = 1;
+  int nt = 1, C = 1, spc = 1, nstages = 1;
   size_t smem = 0;
 };
+
+static int tma_stage_bytes(int nt) {
+  switch (nt) {
+    case 1: return TStage<1>::bytes;
+    case 2: return TStage<2>::bytes;
+    case 3: return TStage<3>::bytes;
+    default: return TStage<4>::bytes;
+  }
+}
 
 // Cluster size: the largest K split (at least two steps per rank) whose CTA
 // count stays within two per SM, so that every CTA is resident at once and
 // the next launch's CTAs still find room to start early (programmatic
 // dependent launch); with many column groups that is one rank per group.
-// Measured on GB300 for N = K = 5120: C = 3 beats 1, 2, 4, 5 and 7.
+// The ranks' partial sums must also fit in rank 0's ring.
+// Measured on GB300 for N = K = 5120, M = 4: C = 3 beats 1, 2, 4, 5 and 7.
 bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
-  if (a.kind != 0 || a.bs != 16 || a.K % 256 != 0 || a.M < 1 || a.M > 8) return false;
+  if (a.kind != 0 || a.bs != 16 || a.K % 256 != 0 || a.M < 1 || a.M > kTMaxM) return false;
   if (a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 30)) return false;
   const DeviceInfo& d = device_info();
+  const int nt = (int)((a.M + 7) / 8);
+  const int stage = tma_stage_bytes(nt);
   const int64_t groups = (a.N + kTRows - 1) / kTRows;
   const int nsteps = (int)(a.K / 256);
   int C = 1;
@@ -964,12 +1017,14 @@ bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
     if (spc < 2) break;
     const int ce = (nsteps + spc - 1) / spc;
     if (groups * ce > 2 * (int64_t)d.sm_count) break;
+    if (ce * kTCons * nt * 512 > std::min(spc, 4) * stage) break;
     C = ce;
   }
   const int spc = (nsteps + C - 1) / C;
   C = (nsteps + spc - 1) / spc;
   const int ns = std::min(spc, 4);
-  const TmaGemvSmem L(ns);
+  const TmaGemvSmem L(ns, stage);
+  pl.nt = nt;
   pl.C = C;
   pl.spc = spc;
   pl.nstages = ns;
@@ -977,7 +1032,7 @@ bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
   return pl.smem <= kFastSmemLimit;
 }
 
-template <int DT>
+template <int DT, int NT>
 int launch_tma_t(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
   CUtensorMap tmW, tmS, tmA;
   const uint64_t S = (uint64_t)a.K / 16;
@@ -1002,9 +1057,9 @@ int launch_tma_t(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
   p.spc = pl.spc;
   p.nstages = pl.nstages;
   p.err = device_error_word();
-  static std::once_flag once[2];
-  std::call_once(once[DT], [] {
-    cudaFuncSetAttribute(gemv_tma<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(gemv_tma<DT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kFastSmemLimit);
   });
   cudaLaunchConfig_t cfg = {};
@@ -1021,16 +1076,31 @@ int launch_tma_t(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tma<DT>, tmW, tmS, tmA, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tma<DT, NT>, tmW, tmS, tmA, p);
   return e == cudaSuccess ? kOk : kCuda;
+}
+
+template <int DT>
+int launch_tma_dt(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
+  switch (pl.nt) {
+    case 1: return launch_tma_t<DT, 1>(a, pl, st);
+    case 2: return launch_tma_t<DT, 2>(a, pl, st);
+    case 3: return launch_tma_t<DT, 3>(a, pl, st);
+    default: return launch_tma_t<DT, 4>(a, pl, st);
+  }
 }
 
 }  // namespace
 
+bool gemv_tma_supports(const GemvArgs& a) {
+  TmaPlan tp;
+  return plan_tma(a, tp);
+}
+
 int launch_gemv(const GemvArgs& a, cudaStream_t st) {
   TmaPlan tp;
   if (plan_tma(a, tp))
-    return a.dtype == 1 ? launch_tma_t<1>(a, tp, st) : launch_tma_t<0>(a, tp, st);
+    return a.dtype == 1 ? launch_tma_dt<1>(a, tp, st) : launch_tma_dt<0>(a, tp, st);
   FastPlan pl;
   if (plan_fast(a, pl)) {
     if (a.kind == 0)

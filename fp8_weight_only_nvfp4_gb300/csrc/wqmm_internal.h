@@ -67,6 +67,8 @@ struct GemvArgs {
   int dtype;
 };
 int launch_gemv(const GemvArgs& a, cudaStream_t st);
+// The TMA decode GEMV also takes 8 < M <= 32 (NVFP4, bs 16, K % 256 == 0).
+bool gemv_tma_supports(const GemvArgs& a);
 
 // ---- fused tcgen05 GEMM for large M (wqmm_gemm.cu) ----
 // Returns kUnsupported if the shape cannot take this path.

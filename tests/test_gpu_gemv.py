@@ -196,3 +196,54 @@ def test_bf16_activation_wide_but_exact_range():
     q = _with_activation(p, A)
     Yr, S = _ref(q)
     assert_within_tolerance(run_fp4(q), Yr, S, q.dtype, "wide exact range")
+
+
+# --- 8 < M <= 32: the TMA decode GEMV with up to four 8-row activation tiles ---
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+@pytest.mark.parametrize("M", [9, 12, 16, 17, 24, 31, 32])
+def test_mid_m_decode_gemv(M, dtype):
+    p = wl.make_fp4(M, 320, 1024, 16, dtype, seed=100 + M, bias_sigma=0.1)
+    Y = run_fp4(p)
+    Yr, S = _ref(p)
+    assert_within_tolerance(Y, Yr, S, dtype, f"mid M={M}")
+
+
+def test_mid_m_5120():
+    """M=16, N=K=5120 (split-K across a cluster), every output."""
+    p = wl.make_fp4(16, 5120, 5120, 16, oracle.BF16, seed=77)
+    Y = run_fp4(p)
+    Yr, S = _ref(p)
+    assert_within_tolerance(Y, Yr, S, p.dtype, "M=16 N=K=5120")
+
+
+def test_one_hot_probe_mid_m():
+    """One-hot activations for M=24 (three activation tiles): Y[m, n] =
+    B_dq[n, k] bit-exact, pinning which lane and tile supply each row."""
+    M, N, K, bs = 24, 48, 256, 16
+    p = wl.make_fp4(M, N, K, bs, oracle.FP16, seed=6, ws2=1.0)
+    d = fp4_dev(p)
+    W = oracle.fp4_dequantize_f64(p.B_packed, p.weight_scale, 1.0, N, K, bs)
+    for k in range(0, K, 5):
+        A = np.zeros((M, K))
+        for m in range(M):
+            A[m, (k + 37 * m) % K] = 1.0
+        d["A"] = act_to_dev(wl.act_bits(A, p.dtype), p.dtype)
+        Y = f64_of(run_fp4(p, d))
+        for m in range(M):
+            assert np.array_equal(Y[m], W[:, (k + 37 * m) % K]), (k, m)
+
+
+def test_rows_independent_mid_m():
+    """Each row of an M=32 batch is bit-identical to the same row computed
+    alone (each activation tile accumulates in its own registers)."""
+    p32 = wl.make_fp4(32, 384, 2048, 16, oracle.BF16, seed=19, bias_sigma=0.1)
+    d = fp4_dev(p32)
+    Y32 = bits_of(run_fp4(p32, d))
+    for m in (0, 7, 8, 15, 16, 23, 24, 31):
+        d1 = dict(d)
+        d1["A"] = d["A"][m:m + 1].contiguous()
+        p1 = wl.Fp4Problem(1, p32.N, p32.K, 16, p32.dtype, p32.A[m:m + 1], p32.B_packed,
+                           p32.weight_scale, p32.weight_scale_2, p32.bias)
+        Y1 = bits_of(run_fp4(p1, d1))
+        assert np.array_equal(Y1[0], Y32[m]), m

@@ -380,13 +380,36 @@ def bench_also(gpu, args, peaks):
             out["comparator_dequant_plus_cublas_ms"] = round((dt_dq + dt_mm) * 1e3, 3)
             del W
         del ly, A, Y
-    # FP8 decode GEMV chain (secondary format), M = 4.
-    step, _, _ = gemv_chain(gpu, 4, 5120, 5120, LAYERS, kind="fp8")
-    g = gpu.graph(step)
+    # FP8 decode GEMV chain (secondary format), M = 1, 4, 8.
     reps = max(5, args.steps // 2)
-    dt = gpu.time_graph(g, reps, 2)
-    gbs = gemv_bytes(4, 5120, 5120, 128, kind="fp8") * LAYERS * reps / dt / 1e9
-    out["fp8_gemv_M4_N5120_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    for M in (1, 4, 8):
+        step, _, _ = gemv_chain(gpu, M, 5120, 5120, LAYERS, kind="fp8")
+        g = gpu.graph(step)
+        dt = gpu.time_graph(g, reps, 2)
+        gbs = gemv_bytes(M, 5120, 5120, 128, kind="fp8") * LAYERS * reps / dt / 1e9
+        out[f"fp8_gemv_M{M}_N5120_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+        del g
+    # Mid-range M (8 < M <= 32) decode GEMV chain, NVFP4.
+    for M in (16, 32):
+        step, _, _ = gemv_chain(gpu, M, 5120, 5120, LAYERS)
+        g = gpu.graph(step)
+        dt = gpu.time_graph(g, reps, 2)
+        gbs = gemv_bytes(M, 5120, 5120) * LAYERS * reps / dt / 1e9
+        out[f"gemv_M{M}_N5120_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                                         "us_per_layer": round(dt / (reps * LAYERS) * 1e6, 2)}
+        del g
+    # FP8 prefill GEMM (secondary format), M = 8192, N = 17408, K = 5120, bs = 128.
+    M, N, K = 8192, 17408, 5120
+    B8 = gpu.t(wl.gen_fp8_weight(N, K, 900))
+    s8 = gpu.t(wl.gen_fp8_scale(N, wl.scale_cols(K, 128), 0.001, 0.02, 900))
+    A = torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+    fn = lambda: wq.fp8_weight_matmul(A, B8, s8, None, 128, out=Y, stream=gpu.stream)
+    dt = gpu.time_each(fn, reps=5, warmup=2)
+    tf = 2 * M * N * K / dt / 1e12
+    out[f"fp8_prefill_M{M}_N{N}_K{K}"] = {"TFLOP/s": round(tf, 1), "frac": round(tf / tf_peak, 4),
+                                          "ms": round(dt * 1e3, 3)}
+    del B8, s8, A, Y
     return out
 
 

@@ -29,6 +29,11 @@
 //              -> registers, * gscale, + bias, one RNE, then Y (through a
 //              shared-memory transpose and one tensor store when the row
 //              pitch allows, else direct stores with lanes = consecutive n).
+//   split-K    when the tiles fill less than half of the GPU (mid-range M
+//              with few weight-row tiles), a cluster of C = 2..4 CTAs along
+//              gridDim.z splits K; the FP32 partial tiles are reduce-
+//              scattered through distributed shared memory (rank b owns
+//              token-column block b and adds the partials in rank order).
 //              Measured: without the tensor-memory stores the kernel runs at
 //              the speed of the plain MMA pipeline; the stores complete late
 //              while the MMA streams, so the four warps of a quarter keep
@@ -170,6 +175,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
 // 8-row core groups 1024 bytes apart (SBO), version field = 1 (sm_100 family).
 __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {
@@ -261,7 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBM;
   const int m0 = blockIdx.y * kBN;
-  const int num_k = (K + kBK - 1) / kBK;
+  const int num_k_all = (K + kBK - 1) / kBK;
+  // Split-K across a cluster of C CTAs along gridDim.z: rank r takes stages
+  // [k_lo, k_lo + num_k) (the host sizes ranks so that every one has some).
+  const int C = gridDim.z;
+  const int rank = blockIdx.z;
+  const int spc = (num_k_all + C - 1) / C;
+  const int k_lo = rank * spc;
+  const int num_k = min(num_k_all, k_lo + spc) - k_lo;
   const int S = (K + bs - 1) / bs;
   constexpr int kWBytes = (KIND == 0) ? kBK / 2 : kBK;  // packed bytes per row per stage
 
@@ -284,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  bool have = false;  // decoder warps: this CTA's accumulator is complete
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -294,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % kStages;
         if (it >= kStages && !wait_bar(&empty[s], ((it / kStages) + 1) & 1, err, abort_flag)) break;
         mbar_arrive_expect_tx(&full[s], bytes);
-        tma_load_2d(smem + L::act + s * kActStageBytes, &tmA, it * kBK, m0, &full[s]);
-        tma_load_2d(smem + L::w + s * L::wstage, &tmW, it * kWBytes, n0, &full[s]);
+        tma_load_2d(smem + L::act + s * kActStageBytes, &tmA, (k_lo + it) * kBK, m0, &full[s]);
+        tma_load_2d(smem + L::w + s * L::wstage, &tmW, (k_lo + it) * kWBytes, n0, &full[s]);
         ++issued;
       }
       // No copy may still be landing in shared memory when the CTA exits:
@@ -354,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fetch = [&](int it, uint32_t (&r)[4]) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int k1 = it * kBK + 16 * c;
+        const int k1 = (k_lo + it) * kBK + 16 * c;
         r[c] = 0u;
         if (n < N && it < num_k && k1 < K) {
           const int col = bs_shift >= 0 ? k1 >> bs_shift : k1 / bs;
@@ -422,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // With a tensor map for Y the tile is staged transposed, [256 tokens x
     // 128 n], in the (now idle) activation ring and written by one tensor
     // store; otherwise each column is stored directly (lanes = consecutive n).
-    const bool have = ok && wait_bar(accfull, 0, err, abort_flag);
-    if (have) {
+    have = ok && wait_bar(accfull, 0, err, abort_flag);
+    if (have && C == 1) {
       tc_fence_after();
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
@@ -445,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (y_tma) {
+    if (y_tma && C == 1) {
       // Make the staged tile visible to the tensor-copy engine, then one
       // elected thread stores it (out-of-range rows and columns are clipped).
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -458,6 +485,80 @@ __global__ void __launch_bounds__(kThreads, 1)
             : "memory");
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      }
+    }
+  }
+
+  // Split-K: reduce-scatter of the FP32 partial tiles through distributed
+  // shared memory.  Token columns are cut into C blocks (multiples of 32);
+  // rank b owns block b: every other rank writes its partial of that block
+  // into rank b's (now idle) activation ring, then rank b adds them in rank
+  // order to its own and runs the epilogue for the block.  Deterministic, no
+  // global scratch.
+  if (C > 1) {
+    __syncwarp();
+    cluster_sync();  // every rank's MMAs are complete and its rings are idle
+    const int wmax = (kBN / C + 31) / 32 * 32;
+    auto block_lo = [&](int bb) { return min(kBN, bb * wmax); };
+    // [C-1 slots][wmax columns][128 rows]: lanes (consecutive rows) write and
+    // read consecutive words, one 128-byte line per warp access.
+    float* recv = reinterpret_cast<float*>(smem + L::act);
+    if (warp >= 2 && have) {
+      const int q = warp & 3, j4 = (warp - 2) >> 2;
+      const int row = q * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      tc_fence_after();
+      for (int bb = 0; bb < C; ++bb) {
+        if (bb == rank) continue;
+        const int c_lo = block_lo(bb), w = block_lo(bb + 1) - c_lo;
+        const int slot = rank < bb ? rank : rank - 1;
+        // This warp: columns [w/4 * j4, w/4 * (j4 + 1)) of the block, 8 at a time.
+        for (int c8 = (w / 4) * j4; c8 < (w / 4) * (j4 + 1); c8 += 8) {
+          uint32_t r[8];
+          tmem_ld8(lane_base + kAccCol + c_lo + c8, r);
+          const uint32_t remote =
+              mapa_shared(smem_u32(recv + ((size_t)slot * wmax + c8) * kBM + row), (uint32_t)bb);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) st_cluster_f32(remote + 4u * kBM * j, __uint_as_float(r[j]));
+        }
+      }
+    }
+    cluster_sync();  // every partial has arrived
+    if (warp >= 2 && have) {
+      const int q = warp & 3, j4 = (warp - 2) >> 2;
+      const int row = q * 32 + lane;
+      const int n = n0 + row;
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      tc_fence_after();
+      const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
+      const float bv = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
+      const int c_lo = block_lo(rank), w = block_lo(rank + 1) - c_lo;
+      for (int c8 = (w / 4) * j4; c8 < (w / 4) * (j4 + 1); c8 += 8) {
+        uint32_t r[8];
+        tmem_ld8(lane_base + kAccCol + c_lo + c8, r);
+        // Rank order: partials of ranks 0 .. C-1, this rank's own in place.
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        for (int src = 0; src < C; ++src) {
+          if (src == rank) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += __uint_as_float(r[j]);
+          } else {
+            const int slot = src < rank ? src : src - 1;
+            const float* pv = recv + ((size_t)slot * wmax + c8) * kBM + row;
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = pv[j * kBM];  // independent loads
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += v[j];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int m = m0 + c_lo + c8 + j;
+          if (n < N && m < M) Y[(int64_t)m * N + n] = to_act_rn<DT>(acc[j] * gs + bv);
+        }
       }
     }
   }
@@ -500,11 +601,43 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
     cudaFuncSetAttribute(gemm_tc_kernel<DT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          GemmCfg<KIND>::smem_bytes);
   });
-  dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)((a.M + kBN - 1) / kBN));
-  gemm_tc_kernel<DT, KIND><<<grid, kThreads, GemmCfg<KIND>::smem_bytes, st>>>(
-      tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale, reinterpret_cast<const uint16_t*>(a.bias),
-      reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, a.bs, device_error_word());
-  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+  // Split-K (cluster of C CTAs along z) when the tiles fill less than half
+  // of the GPU: each rank decodes and multiplies 1/C of K, one CTA per SM.
+  const int64_t tiles_n = (a.N + kBM - 1) / kBM, tiles_m = (a.M + kBN - 1) / kBN;
+  const int64_t tiles = tiles_n * tiles_m;
+  const int num_k = (int)((a.K + kBK - 1) / kBK);
+  const int sms = device_info().sm_count;
+  int C = 1;
+  if (tiles * 2 <= sms) {
+    for (int c = 4; c >= 2; --c) {
+      if (tiles * c <= sms && num_k >= 8 * c) {
+        C = c;
+        break;
+      }
+    }
+    if (C > 1) {
+      const int spc = (num_k + C - 1) / C;
+      C = (num_k + spc - 1) / spc;
+    }
+  }
+  const dim3 grid((unsigned)tiles_n, (unsigned)tiles_m, (unsigned)C);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = GemmCfg<KIND>::smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)C;
+  cfg.attrs = attr;
+  cfg.numAttrs = C > 1 ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, gemm_tc_kernel<DT, KIND>, tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale,
+      reinterpret_cast<const uint16_t*>(a.bias), reinterpret_cast<uint16_t*>(a.Y), (int)a.M,
+      (int)a.N, (int)a.K, a.bs, device_error_word());
+  return e == cudaSuccess ? kOk : kCuda;
 }
 
 }  // namespace

@@ -97,3 +97,48 @@ def test_fp8_tail_prefill_sampled():
         return oracle.fp8_matmul_sampled(p.A, p.B, p.b_scale, p.bias, p.K, p.block_size,
                                          p.dtype, ms, ns)
     _sampled_check(p, run_fp8, ref, n_random=2048, full_rows=2, full_cols=2)
+
+
+# --- split-K: a thread-block cluster splits K, partial tiles reduce-scattered
+# --- through distributed shared memory (used when the tiles fill < half the GPU)
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+@pytest.mark.parametrize("M,N,K,bs", [
+    (40, 384, 2048, 16),    # 3 tiles: 4 ranks
+    (100, 640, 1600, 16),   # 5 tiles, 25 stages: 3 ranks of 9, 9, 7 stages
+    (200, 128, 17408, 16),  # 1 tile, long K: 4 ranks
+    (33, 256, 4096, 32),
+])
+def test_split_k_shapes(M, N, K, bs, dtype):
+    p = wl.make_fp4(M, N, K, bs, dtype, seed=M + N + K, bias_sigma=0.05)
+    assert_within_tolerance(run_fp4(p), *_ref(p), dtype, f"split-K {M}x{N}x{K}")
+
+
+def test_split_k_5120_full():
+    """M=64, N=K=5120 (40 tiles, 3 ranks): every output."""
+    p = wl.make_fp4(64, 5120, 5120, 16, oracle.BF16, seed=64, bias_sigma=0.02)
+    assert_within_tolerance(run_fp4(p), *_ref(p), p.dtype, "split-K 64x5120x5120")
+
+
+def test_one_hot_probe_split_k():
+    """One-hot probe through the split-K path (K=2048: 4 ranks), bit-exact:
+    each token's single product lives in one rank's partial and crosses the
+    reduce-scatter unchanged."""
+    M, N, K, bs = 64, 128, 2048, 16
+    p = wl.make_fp4(M, N, K, bs, oracle.FP16, seed=23, ws2=1.0)
+    d = fp4_dev(p)
+    W = oracle.fp4_dequantize_f64(p.B_packed, p.weight_scale, 1.0, N, K, bs)
+    for shift in (0, 555, 1999):
+        ks = (np.arange(M) * 31 + shift) % K
+        A = np.zeros((M, K))
+        A[np.arange(M), ks] = 1.0
+        d["A"] = act_to_dev(wl.act_bits(A, p.dtype), p.dtype)
+        Y = f64_of(run_fp4(p, d))
+        assert np.array_equal(Y, W[:, ks].T), shift
+
+
+def test_fp8_split_k():
+    p = wl.make_fp8(48, 256, 4096, 128, oracle.BF16, seed=48, bias_sigma=0.05)
+    Y = run_fp8(p)
+    Yr, S = oracle.fp8_matmul(p.A, p.B, p.b_scale, p.bias, p.M, p.N, p.K, p.block_size, p.dtype)
+    assert_within_tolerance(Y, Yr, S, p.dtype, "fp8 split-K")

@@ -342,6 +342,25 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Two E4M3 bytes (low 16 bits) -> the same values as an operand pair, exact
+// (4 significant bits): FP16 straight from the convert, BF16 through two
+// exact FP32 widenings and a pack.
+template <int DT>
+__device__ __forceinline__ uint32_t e4m3x2_exact(uint32_t two) {
+  const uint32_t h = e4m3x2_to_f16x2(two);
+  if constexpr (DT == 0) {
+    return h;
+  } else {
+    float lo, hi;
+    asm("{ .reg .b16 l, u; mov.b32 {l, u}, %2;\n\t"
+        "cvt.f32.f16 %0, l; cvt.f32.f16 %1, u; }"
+        : "=f"(lo), "=f"(hi) : "r"(h));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+}
+
 // FP8: two E4M3 bytes (low 16 bits) times a float scale -> operand pair,
 // rounded once to the activation type.
 template <int DT>
@@ -410,15 +429,27 @@ __device__ __forceinline__ void chunk_load(Chunk<DT, KIND>& c, const FastParams&
         const uint8_t* r = p.B + (int64_t)row0 * p.K + k0;
         c.w0[i][0] = ldg_stream_v4(r);
         c.w0[i][1] = ldg_stream_v4(r + 16);
-        c.f0[i][0] = __ldg(p.fscale + (int64_t)row0 * S + sa);
-        c.f0[i][1] = __ldg(p.fscale + (int64_t)row0 * S + sb);
       }
       if (v1) {
         const uint8_t* r = p.B + (int64_t)row1 * p.K + k0;
         c.w1[i][0] = ldg_stream_v4(r);
         c.w1[i][1] = ldg_stream_v4(r + 16);
-        c.f1[i][0] = __ldg(p.fscale + (int64_t)row1 * S + sa);
-        c.f1[i][1] = __ldg(p.fscale + (int64_t)row1 * S + sb);
+      }
+      if (p.bs_shift >= 7) {
+        // One block per window: its scale, whatever part of the window this
+        // lane's 32-k run covers (the MMA mixes the four lanes' runs).
+        const int sw = (w * 128) >> p.bs_shift;
+        if (w < win_end && row0 < p.N) c.f0[i][0] = __ldg(p.fscale + (int64_t)row0 * S + sw);
+        if (w < win_end && row1 < p.N) c.f1[i][0] = __ldg(p.fscale + (int64_t)row1 * S + sw);
+      } else {
+        if (v0) {
+          c.f0[i][0] = __ldg(p.fscale + (int64_t)row0 * S + sa);
+          c.f0[i][1] = __ldg(p.fscale + (int64_t)row0 * S + sb);
+        }
+        if (v1) {
+          c.f1[i][0] = __ldg(p.fscale + (int64_t)row1 * S + sa);
+          c.f1[i][1] = __ldg(p.fscale + (int64_t)row1 * S + sb);
+        }
       }
     }
   }
@@ -427,7 +458,8 @@ __device__ __forceinline__ void chunk_load(Chunk<DT, KIND>& c, const FastParams&
 template <int DT, int KIND>
 __device__ __forceinline__ void chunk_compute(float (&acc)[4], const Chunk<DT, KIND>& c,
                                               const uint8_t* act_row, bool act_on, int k_lo,
-                                              int win_begin, int win_end, int t) {
+                                              int win_begin, int win_end, int t,
+                                              bool block_is_window) {
   constexpr int kWpc = wpc_of<KIND>();
 #pragma unroll
   for (int i = 0; i < kWpc; ++i) {
@@ -468,6 +500,26 @@ __device__ __forceinline__ void chunk_compute(float (&acc)[4], const Chunk<DT, K
                     x[2 * j], x[2 * j + 1], DT);
         }
       }
+    } else if (block_is_window) {
+      // One scale block per row and window (bs >= 128): the window's MMAs
+      // take the E4M3 values themselves (exact in FP16 and BF16) into a fresh
+      // accumulator, which is then scaled by the rows' block scales in FP32:
+      // one convert per weight pair for FP16 activations, and the weight is
+      // never rounded after scaling.
+      float w4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 q0 = c.w0[i][j >> 2], q1 = c.w1[i][j >> 2];
+        const uint32_t wv0 = ((const uint32_t*)&q0)[j & 3];
+        const uint32_t wv1 = ((const uint32_t*)&q1)[j & 3];
+        const uint32_t a0 = e4m3x2_exact<DT>(wv0 & 0xFFFF), a2 = e4m3x2_exact<DT>(wv0 >> 16);
+        const uint32_t a1 = e4m3x2_exact<DT>(wv1 & 0xFFFF), a3 = e4m3x2_exact<DT>(wv1 >> 16);
+        mma_16816(w4, a0, a1, a2, a3, x[2 * j], x[2 * j + 1], DT);
+      }
+      acc[0] = fmaf(w4[0], c.f0[i][0], acc[0]);
+      acc[1] = fmaf(w4[1], c.f0[i][0], acc[1]);
+      acc[2] = fmaf(w4[2], c.f1[i][0], acc[2]);
+      acc[3] = fmaf(w4[3], c.f1[i][0], acc[3]);
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -540,14 +592,15 @@ __global__ void __launch_bounds__(kFastWarps * 32, 2) gemv_fast(const FastParams
 
   constexpr int kWpc = wpc_of<KIND>();
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const bool block_is_window = KIND == 1 && p.bs_shift >= 7;
   const bool act_on = g < p.M;
   const uint8_t* act_row = act + (act_on ? g : 0) * p.act_pitch;
   for (int wb = win_lo; wb < win_hi; wb += 2 * kWpc) {
     if (wb + kWpc < win_hi) chunk_load<DT, KIND>(c1, p, row0, row1, wb + kWpc, win_hi, t);
-    chunk_compute<DT, KIND>(acc, c0, act_row, act_on, k_lo, wb, win_hi, t);
+    chunk_compute<DT, KIND>(acc, c0, act_row, act_on, k_lo, wb, win_hi, t, block_is_window);
     if (wb + 2 * kWpc < win_hi) chunk_load<DT, KIND>(c0, p, row0, row1, wb + 2 * kWpc, win_hi, t);
     if (wb + kWpc < win_hi)
-      chunk_compute<DT, KIND>(acc, c1, act_row, act_on, k_lo, wb + kWpc, win_hi, t);
+      chunk_compute<DT, KIND>(acc, c1, act_row, act_on, k_lo, wb + kWpc, win_hi, t, block_is_window);
   }
 
   if (C > 1) {

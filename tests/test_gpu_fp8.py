@@ -29,7 +29,11 @@ def test_fp8_tail_k5000(M):
 
 @pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
 @pytest.mark.parametrize("M,N,K,bs", [(3, 40, 1000, 128), (8, 17, 48, 16), (2, 64, 4096, 64),
-                                      (5, 33, 130, 32)])
+                                      (5, 33, 130, 32),
+                                      # block scale applied per 128-k window after the MMAs:
+                                      # partial last window, and blocks spanning two windows
+                                      (4, 96, 4064, 128), (7, 130, 1056, 128), (6, 72, 2048, 256),
+                                      (1, 64, 8192, 512)])
 def test_fp8_shapes(M, N, K, bs, dtype):
     p = wl.make_fp8(M, N, K, bs, dtype, seed=K, bias_sigma=0.1)
     assert_within_tolerance(run_fp8(p), *_ref(p), dtype, f"fp8 {M}x{N}x{K}")

@@ -398,6 +398,13 @@ def bench_also(gpu, args, peaks):
         out[f"gemv_M{M}_N5120_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
                                          "us_per_layer": round(dt / (reps * LAYERS) * 1e6, 2)}
         del g
+    # Whole decode step: one CUDA graph of 120 weight-only GEMVs shaped like a
+    # 27B-class decoder (hidden 5120, MLP 17408): per layer four 5120 x 5120
+    # projections, gate and up 17408 x 5120, down 5120 x 17408 (17 layers), then
+    # the 152064 x 5120 lm_head; distinct synthetic weights per launch (3.6 GB,
+    # far above L2).  Only the matmuls are timed: the attention core and the
+    # activation function between them are not part of this path.
+    out.update(decode_step(gpu, (4, 1), reps=max(3, args.steps // 10)))
     # FP8 prefill GEMM (secondary format), M = 8192, N = 17408, K = 5120, bs = 128.
     M, N, K = 8192, 17408, 5120
     B8 = gpu.t(wl.gen_fp8_weight(N, K, 900))
@@ -411,6 +418,48 @@ def bench_also(gpu, args, peaks):
                                           "ms": round(dt * 1e3, 3)}
     del B8, s8, A, Y
     return out
+
+
+def decode_step(gpu, Ms, reps, layers=17, hidden=5120, mlp=17408, vocab=152064):
+    """120 chained GEMV launches of a synthetic 27B-class decode step, for
+    each M in Ms (same weights)."""
+    torch = gpu.torch
+    wq = gpu.wq
+    shapes = []
+    for _ in range(layers):
+        shapes += [(hidden, hidden)] * 4 + [(mlp, hidden), (mlp, hidden), (hidden, mlp)]
+    shapes.append((vocab, hidden))
+    ws = [gpu.fp4_layers(1, N, K, 1, seed0=2000 + i)[0] for i, (N, K) in enumerate(shapes)]
+    res = {}
+    for M in Ms:
+        x_h = gpu.t(wl.gen_activation(M, hidden, 1, 11).view(np.int16), torch.bfloat16)
+        bufs = {hidden: [x_h, torch.empty(M, hidden, dtype=torch.bfloat16, device=gpu.dev)],
+                mlp: [torch.empty(M, mlp, dtype=torch.bfloat16, device=gpu.dev) for _ in range(2)],
+                vocab: [torch.empty(M, vocab, dtype=torch.bfloat16, device=gpu.dev)]}
+
+        def step():
+            cur = bufs[hidden][0]
+            for i, ((N, K), ly) in enumerate(zip(shapes, ws)):
+                y = bufs[N][i % len(bufs[N])]
+                if y is cur:
+                    y = bufs[N][(i + 1) % len(bufs[N])]
+                wq.fp4_weight_matmul(cur, ly["B"], ly["ws"], ly["ws2"], None, 16, out=y,
+                                     stream=gpu.stream)
+                # q, k, v, o, up and down feed the next launch; gate's output
+                # is not consumed (up's output feeds down)
+                if i >= 7 * layers or i % 7 != 4:
+                    cur = y
+        g = gpu.graph(step)
+        dt = gpu.time_graph(g, reps, 2)
+        per_step = dt / reps
+        byts = sum(gemv_bytes(M, N, K) for (N, K) in shapes)
+        res[f"decode_step_M{M}_{len(shapes)}_gemv"] = {
+            "us_per_step": round(per_step * 1e6, 1), "GB/s": round(byts / per_step / 1e9, 1),
+            "frac": round(byts / per_step / 1e9 / load_peaks()["hbm_gbs"], 4),
+            "weight_GB": round(byts / 1e9, 2)}
+        del g
+    del ws
+    return res
 
 
 def cpu_oracle_baseline(budget_s=10.0):
@@ -519,6 +568,9 @@ def run_only(name, m, reps):
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
         fn = lambda: wq.fp8_weight_matmul(A, B, sc, None, 128, out=Y, stream=gpu.stream)
         work = gemv_bytes(M, N, K, 128, kind="fp8") / 1e9, "GB/s"
+    elif name == "decode_step":
+        print(json.dumps(decode_step(gpu, (m or 4,), reps=reps)), flush=True)
+        return
     else:
         raise SystemExit(f"unknown workload {name}")
     dt = gpu.time_each(fn, reps=reps, warmup=2, flush=True)
@@ -536,7 +588,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--only", default=None,
                     help="run one workload (gemv, lm_head, prefill_gate_up, prefill_down, "
-                         "dequant, fp8_gemv) a few times, for profilers")
+                         "dequant, fp8_gemv, decode_step) a few times, for profilers")
     ap.add_argument("--m", type=int, default=None, help="rows of A for --only")
     ap.add_argument("--reps", type=int, default=3, help="timed launches for --only")
     args = ap.parse_args()

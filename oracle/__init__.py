@@ -85,6 +85,9 @@ def _load():
         lib.orc_fp8_matmul.argtypes = [P, P, P, P, I64, I64, I64, I, I, P, P, I]
         lib.orc_fp4_matmul_sampled.argtypes = [P, P, P, F, P, I64, I, I, P, P, I64, P, P, I]
         lib.orc_fp8_matmul_sampled.argtypes = [P, P, P, P, I64, I, I, P, P, I64, P, P, I]
+        lib.orc_e4m3_from_f32.argtypes = [F]
+        lib.orc_e4m3_from_f32.restype = I
+        lib.orc_fp8_qdq_activation.argtypes = [P, F, P, I64, I]
         _lib = lib
         return lib
 
@@ -111,6 +114,21 @@ def e2m1_value(code: int) -> float:
 
 def e4m3_value(byte: int) -> float:
     return float(_load().orc_e4m3_value(int(byte)))
+
+
+def e4m3_from_f32(f: float) -> int:
+    """E4M3FN code of a float32 value: RNE, ties to even, saturating at 448."""
+    return int(_load().orc_e4m3_from_f32(float(np.float32(f))))
+
+
+def fp8_qdq_activation(A, a_scale: float, dtype: int) -> np.ndarray:
+    """W8A8 activation path (FP8 page §6): RNE_act(fp32(e4m3(fp32(A / a_scale)) *
+    a_scale)) per element; A and the result are activation bit patterns."""
+    a = _c(A, np.uint16)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().orc_fp8_qdq_activation(_ptr(a), float(np.float32(a_scale)), _ptr(out), a.size,
+                                   int(dtype))
+    return out
 
 
 def rne_f32_to_act(f32: np.ndarray, dtype: int) -> np.ndarray:

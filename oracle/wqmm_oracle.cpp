@@ -25,6 +25,12 @@
 //   * matmul reference: exact decode in float64, float64 sums, bias added in
 //     float64; the tolerance is applied by the caller.
 //
+//   * W8A8 activation quantization ([FP8] §6, "Optional W8A8 Activation
+//     Path": A_deq = fp8_e4m3(A / a_scale) * a_scale): A / a_scale as one
+//     float32 division (IEEE, correctly rounded), E4M3FN by round-to-nearest-
+//     even with saturation to +-448 (NaN stays NaN), the product with a_scale
+//     as one float32 multiplication, then RNE to the activation type.
+//
 // Parity pins for every function here live in tests/test_oracle_pins.py.
 
 #include <cmath>
@@ -240,6 +246,36 @@ void matmul_sampled(const uint16_t* A, const uint16_t* bias, int64_t K,
 
 }  // namespace
 
+// E4M3FN code of a float32 value: round to nearest, ties to the even
+// mantissa, saturating to the largest finite magnitude 448; NaN -> 0x7F with
+// the input's sign.  Plain table search over the 127 non-negative finite
+// codes (0x00 .. 0x7E ascend in value).
+uint8_t e4m3_rne_satfinite(float f) {
+  build_e4m3_table();
+  const uint8_t sign = std::signbit(f) ? 0x80 : 0x00;
+  if (std::isnan(f)) return (uint8_t)(sign | 0x7F);
+  const double a = std::fabs((double)f);
+  if (a >= g_e4m3[0x7E]) return (uint8_t)(sign | 0x7E);
+  int lo = 0;
+  while (lo + 1 <= 0x7E && g_e4m3[lo + 1] <= a) ++lo;  // g[lo] <= a < g[lo + 1]
+  if (g_e4m3[lo] == a) return (uint8_t)(sign | lo);
+  const double dlo = a - g_e4m3[lo], dhi = g_e4m3[lo + 1] - a;
+  int c;
+  if (dlo < dhi) c = lo;
+  else if (dhi < dlo) c = lo + 1;
+  else c = (lo % 2 == 0) ? lo : lo + 1;  // tie: even mantissa (code parity = mantissa parity)
+  return (uint8_t)(sign | c);
+}
+
+// One activation element of the W8A8 path: RNE_act(fp32(e4m3(fp32(a / s)) * s)).
+uint16_t fp8_qdq_one(uint16_t a_bits, float a_scale, int dtype) {
+  const float a = (float)act_to_double(a_bits, dtype);     // exact
+  const float q = a / a_scale;                               // one float32 division
+  const uint8_t code = e4m3_rne_satfinite(q);
+  const float v = (float)g_e4m3[code] * a_scale;             // one float32 multiplication
+  return rne_to_act(f32_bits(v), dtype);
+}
+
 extern "C" {
 
 int orc_hardware_threads(void) {
@@ -259,6 +295,15 @@ void orc_rne_f32_to_act_array(const uint32_t* in, uint16_t* out, int64_t n, int 
 }
 
 double orc_act_to_double(uint16_t bits, int dtype) { return act_to_double(bits, dtype); }
+
+int orc_e4m3_from_f32(float f) { return e4m3_rne_satfinite(f); }
+
+// W8A8 activation quantize-dequantize ([FP8] §6), element by element.
+void orc_fp8_qdq_activation(const uint16_t* A, float a_scale, uint16_t* out, int64_t n,
+                            int dtype) {
+  build_e4m3_table();
+  for (int64_t i = 0; i < n; ++i) out[i] = fp8_qdq_one(A[i], a_scale, dtype);
+}
 
 // Standalone FP4 dequantize (bit-exact contract):
 //   t = fp32(e2m1 * e4m3)        -- exact

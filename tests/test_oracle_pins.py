@@ -370,3 +370,60 @@ def test_tolerance_formula():
     S = np.array([0.0, 1.0, 100.0])
     assert np.allclose(oracle.tolerance(S, oracle.BF16), [1e-3, 9e-3, 0.801])
     assert np.allclose(oracle.tolerance(S, oracle.FP16), [1e-4, 2.1e-3, 0.2001])
+
+
+# --- W8A8 activation path (FP8 page §6: A_deq = fp8_e4m3(A / a_scale) * a_scale) ---
+
+def test_e4m3_encode_roundtrip_every_code():
+    """Every finite E4M3FN value encodes back to its own code (+-0 keep their sign)."""
+    for c in list(range(0x00, 0x7F)) + list(range(0x80, 0xFF)):
+        v = np.float32(oracle.e4m3_value(c))
+        assert oracle.e4m3_from_f32(v) == c, hex(c)
+
+
+def test_e4m3_encode_ties_to_even_and_nearest():
+    """Midpoints between neighbouring codes go to the even code; a hair off a
+    midpoint goes to the nearer one (all 126 positive gaps, and negated)."""
+    for c in range(0x00, 0x7E):
+        lo, hi = oracle.e4m3_value(c), oracle.e4m3_value(c + 1)
+        mid = np.float32((lo + hi) / 2)      # exact: one bit more than the codes
+        assert float(mid) == (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_from_f32(mid) == even, hex(c)
+        assert oracle.e4m3_from_f32(-mid) == 0x80 | even, hex(c)
+        below = np.nextafter(mid, np.float32(-np.inf))
+        above = np.nextafter(mid, np.float32(np.inf))
+        assert oracle.e4m3_from_f32(below) == c, hex(c)
+        assert oracle.e4m3_from_f32(above) == c + 1, hex(c)
+
+
+def test_e4m3_encode_saturation_and_nan():
+    for v in (448.0, 449.0, 464.0, 480.0, 1e30, np.inf):
+        assert oracle.e4m3_from_f32(v) == 0x7E
+        assert oracle.e4m3_from_f32(-v) == 0xFE
+    assert oracle.e4m3_from_f32(np.nan) & 0x7F == 0x7F
+    assert oracle.e4m3_from_f32(2.0 ** -10) == 0x00        # half the smallest subnormal: tie -> 0
+    assert oracle.e4m3_from_f32(1.5 * 2.0 ** -10) == 0x01  # nearer to 2^-9
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """Library cross-check: torch's float32 -> float8_e4m3fn conversion (its
+    own implementation, round to nearest even) agrees on in-range values."""
+    torch = pytest.importorskip("torch")
+    r = np.random.Generator(np.random.PCG64(12))
+    v = np.concatenate([r.uniform(-448, 448, 20000), r.normal(0, 1, 20000),
+                        r.normal(0, 1e-2, 5000)]).astype(np.float32)
+    t = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    o = np.array([oracle.e4m3_from_f32(x) for x in v], dtype=np.uint8)
+    assert np.array_equal(t, o)
+
+
+def test_fp8_qdq_activation_hand_cases():
+    """Hand-computed W8A8 activation rounding (a_scale = 2): 6.5 / 2 = 3.25 is
+    an E4M3 value; 6.75 / 2 = 3.375 is the midpoint of 3.25 and 3.5 and goes
+    to the even mantissa 3.5 -> 7.0; 1000 / 2 saturates at 448 -> 896; 0 stays."""
+    for dtype in (oracle.BF16, oracle.FP16):
+        A = wl.act_bits(np.array([6.5, 6.75, -6.75, 1000.0, 0.0]), dtype)
+        out = oracle.fp8_qdq_activation(A, 2.0, dtype)
+        got = [oracle.act_to_double(int(b), dtype) for b in out]
+        assert got == [6.5, 7.0, -7.0, 896.0, 0.0], (dtype, got)

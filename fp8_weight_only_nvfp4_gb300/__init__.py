@@ -15,6 +15,9 @@ Torch-tensor wrappers (same names):
   ("MatMulBlockQuantizedFp4Weight - CUDA Operator Documentation" §1).
 * ``fp8_weight_matmul(A, B, b_scale, bias=None, block_size=128, out=None)``
   ("MatMulBlockQuantizedFp8Weight - CUDA Operator Documentation" §1).
+* ``fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias=None, block_size=128, out=None)``
+  and ``fp8_quantize_dequantize_activation(A, a_scale)`` ("MatMulBlockQuantizedFp8Weight -
+  CUDA Operator Documentation" §6, the optional W8A8 activation path).
 * ``fp4_dequantize(B_packed, weight_scale, weight_scale_2, block_size=16,
   dtype=torch.bfloat16, out=None)`` and ``fp8_dequantize(...)``.
 """
@@ -27,6 +30,7 @@ import threading
 
 __all__ = [
     "WqmmError", "lib", "library_path", "fp4_weight_matmul", "fp8_weight_matmul",
+    "fp8_weight_matmul_w8a8", "fp8_quantize_dequantize_activation",
     "fp4_dequantize", "fp8_dequantize", "device_status", "FP16", "BF16",
 ]
 
@@ -44,7 +48,8 @@ STATUS = {
 }
 
 # Exported C symbols, in header order.
-SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp4_dequantize", "fp8_dequantize",
+SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
+           "fp8_quantize_dequantize_activation", "fp4_dequantize", "fp8_dequantize",
            "wqmm_status_string", "wqmm_device_status", "wqmm_version")
 
 
@@ -73,13 +78,16 @@ def lib():
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.fp4_weight_matmul.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P]
         L.fp8_weight_matmul.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
+        L.fp8_weight_matmul_w8a8.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P]
+        L.fp8_quantize_dequantize_activation.argtypes = [P, P, P, I64, I, P]
         L.fp4_dequantize.argtypes = [P, P, P, P, I64, I64, I, I, P]
         L.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, I, P]
         L.wqmm_status_string.argtypes = [I]
         L.wqmm_status_string.restype = ctypes.c_char_p
         L.wqmm_device_status.argtypes = [P]
         L.wqmm_version.argtypes = []
-        for name in ("fp4_weight_matmul", "fp8_weight_matmul", "fp4_dequantize",
+        for name in ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
+                     "fp8_quantize_dequantize_activation", "fp4_dequantize",
                      "fp8_dequantize", "wqmm_device_status", "wqmm_version"):
             getattr(L, name).restype = I
         _lib = L
@@ -128,6 +136,11 @@ def _need_cuda(*ts):
                 raise ValueError("all tensors must be contiguous")
 
 
+def _need_scale(a_scale):
+    if a_scale.dtype != _torch().float32 or a_scale.numel() != 1:
+        raise ValueError("a_scale must be a one-element float32 tensor")
+
+
 def fp4_weight_matmul(A, B_packed, weight_scale, weight_scale_2, bias=None, block_size=16,
                       out=None, stream=None):
     torch = _torch()
@@ -158,6 +171,39 @@ def fp8_weight_matmul(A, B, b_scale, bias=None, block_size=128, out=None, stream
     st = lib().fp8_weight_matmul(_ptr(A), _ptr(B), _ptr(b_scale), _ptr(bias), _ptr(out), M, N,
                                  K, int(block_size), _dt(A.dtype), _stream(stream))
     _check(st, "fp8_weight_matmul")
+    return out
+
+
+def fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias=None, block_size=128, out=None,
+                           stream=None):
+    """FP8 page §6 W8A8 path: Y = (fp8_e4m3(A / a_scale) * a_scale) * dequant(B)^T (+ bias).
+    a_scale is a one-element float32 CUDA tensor."""
+    torch = _torch()
+    _need_cuda(A, a_scale, B, b_scale, bias, out)
+    _need_scale(a_scale)
+    N, K = B.shape
+    if A.shape[-1] != K:
+        raise ValueError(f"A.shape[-1]={A.shape[-1]} != K={K}")
+    M = A.numel() // K if K else int(torch.tensor(A.shape[:-1]).prod())
+    if out is None:
+        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=A.device)
+    st = lib().fp8_weight_matmul_w8a8(_ptr(A), _ptr(a_scale), _ptr(B), _ptr(b_scale), _ptr(bias),
+                                      _ptr(out), M, N, K, int(block_size), _dt(A.dtype),
+                                      _stream(stream))
+    _check(st, "fp8_weight_matmul_w8a8")
+    return out
+
+
+def fp8_quantize_dequantize_activation(A, a_scale, out=None, stream=None):
+    """A_deq = fp8_e4m3(A / a_scale) * a_scale, elementwise (bit-exact contract)."""
+    _need_cuda(A, a_scale, out)
+    _need_scale(a_scale)
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(A)
+    st = lib().fp8_quantize_dequantize_activation(_ptr(A), _ptr(a_scale), _ptr(out), A.numel(),
+                                                  _dt(A.dtype), _stream(stream))
+    _check(st, "fp8_quantize_dequantize_activation")
     return out
 
 

@@ -204,6 +204,60 @@ int fp8_weight_matmul(const void* A, const uint8_t* B, const float* b_scale, con
   return matmul_common(a, static_cast<cudaStream_t>(stream));
 }
 
+int fp8_weight_matmul_w8a8(const void* A, const float* a_scale, const uint8_t* B,
+                           const float* b_scale, const void* bias, void* Y, int64_t M,
+                           int64_t N, int64_t K, int block_size, int dtype, void* stream) {
+  int r = check_common(M, N, K, block_size, dtype);
+  if (r != WQMM_OK) return r;
+  if (block_size % 16 != 0) return WQMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return WQMM_OK;
+  if (!Y) return WQMM_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B || !b_scale || !a_scale)) return WQMM_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (A && !aligned16(A)) || (B && !aligned16(B)) ||
+      (b_scale && !aligned16(b_scale)) || (a_scale && !aligned_n(a_scale, 4)) ||
+      (bias && !aligned_n(bias, 2)))
+    return WQMM_ERR_MISALIGNED;
+  if (current_device() < 0) return WQMM_ERR_CUDA;
+  GemvArgs a{};
+  a.kind = 1;
+  a.A = A;
+  a.B = B;
+  a.fscale = b_scale;
+  a.ascale = a_scale;
+  a.bias = bias;
+  a.Y = Y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bs = block_size;
+  a.dtype = dtype;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_fill_bias(bias, Y, M, N, dtype, st);
+  // The activation is rounded where the GEMV stages it; the GEMM has no such
+  // step, so every M runs the GEMV (per group of 8 rows above that).
+  for (int64_t m0 = 0; m0 < M; m0 += 8) {
+    GemvArgs b = a;
+    b.M = std::min<int64_t>(8, M - m0);
+    b.A = static_cast<const char*>(A) + m0 * K * 2;
+    b.Y = static_cast<char*>(Y) + m0 * N * 2;
+    const int rr = launch_gemv(b, st);
+    if (rr != WQMM_OK) return rr;
+  }
+  return WQMM_OK;
+}
+
+int fp8_quantize_dequantize_activation(const void* A, const float* a_scale, void* out,
+                                       int64_t count, int dtype, void* stream) {
+  if (dtype != WQMM_FP16 && dtype != WQMM_BF16) return WQMM_ERR_INVALID_ARG;
+  if (count < 0) return WQMM_ERR_INVALID_ARG;
+  if (count == 0) return WQMM_OK;
+  if (!A || !a_scale || !out) return WQMM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(out) || !aligned_n(a_scale, 4)) return WQMM_ERR_MISALIGNED;
+  if (current_device() < 0) return WQMM_ERR_CUDA;
+  return launch_fp8_qdq_activation(A, a_scale, out, count, dtype,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 int fp4_dequantize(const uint8_t* B_packed, const uint8_t* weight_scale,
                    const float* weight_scale_2, void* out, int64_t N, int64_t K, int block_size,
                    int dtype, void* stream) {

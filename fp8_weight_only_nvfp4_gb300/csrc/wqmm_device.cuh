@@ -250,6 +250,40 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return r;
 }
 
+// W8A8 activation path ("MatMulBlockQuantizedFp8Weight - CUDA Operator
+// Documentation" §6): A_deq = fp8_e4m3(A / a_scale) * a_scale, for a pair of
+// activation values (low half = first).  The division is IEEE float32
+// (correctly rounded), the E4M3 conversion rounds to nearest even and
+// saturates at +-448 (NaN stays NaN), the product is one float32 rounding,
+// then one RNE to the activation type.
+template <int DT>
+__device__ __forceinline__ float act_bits_to_f32(uint32_t bits16) {
+  if constexpr (DT == 1) return __uint_as_float(bits16 << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t qdq_fp8_act_pair(uint32_t two, float a_scale) {
+  const float lo = __fdiv_rn(act_bits_to_f32<DT>(two & 0xFFFFu), a_scale);
+  const float hi = __fdiv_rn(act_bits_to_f32<DT>(two >> 16), a_scale);
+  uint32_t q;
+  asm("{ .reg .b16 c; cvt.rn.satfinite.e4m3x2.f32 c, %2, %1; cvt.u32.u16 %0, c; }"
+      : "=r"(q) : "f"(lo), "f"(hi));
+  uint32_t h;
+  asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(h) : "r"(q));
+  const float dlo = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  const float dhi = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+  uint32_t r;
+  if constexpr (DT == 1) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(__fmul_rn(dlo, a_scale), __fmul_rn(dhi, a_scale));
+    r = *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(__fmul_rn(dlo, a_scale), __fmul_rn(dhi, a_scale));
+    r = *reinterpret_cast<uint32_t*>(&v);
+  }
+  return r;
+}
+
 // One E4M3 byte -> float (exact).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   const uint32_t h2 = e4m3x2_to_f16x2(byte & 0xFFu);

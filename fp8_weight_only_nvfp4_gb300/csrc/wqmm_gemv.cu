@@ -200,9 +200,11 @@ template <int DT, int KIND, bool ALIGNED>
 __global__ void __launch_bounds__(kGemvWarps * 32)
     gemv_general(const uint16_t* __restrict__ A, const uint8_t* __restrict__ B,
                  const uint8_t* __restrict__ ws, const float* __restrict__ gscale,
-                 const float* __restrict__ fscale, const uint16_t* __restrict__ bias,
-                 uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K, int bs) {
+                 const float* __restrict__ fscale, const float* __restrict__ ascale,
+                 const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int64_t M,
+                 int64_t N, int64_t K, int bs) {
   __shared__ float red[kGemvWarps][4][32];
+  const float a_s = ascale != nullptr ? __ldg(ascale) : 1.f;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -218,6 +220,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
     const int64_t k0 = win * 128 + 32 * t;
     uint32_t x[16];
     load_act<ALIGNED>(A, M, K, m, k0, x);
+    if (ascale != nullptr) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = qdq_fp8_act_pair<DT>(x[i], a_s);
+    }
     if constexpr (KIND == 0) {
       const uint4 pb0 = load_fp4_row<ALIGNED>(B, N, K, r0, k0);
       const uint4 pb1 = load_fp4_row<ALIGNED>(B, N, K, r1, k0);
@@ -283,10 +289,10 @@ int launch_general_t(const GemvArgs& a, cudaStream_t st) {
   uint16_t* Y = reinterpret_cast<uint16_t*>(a.Y);
   if (aligned)
     gemv_general<DT, KIND, true><<<grid, kGemvWarps * 32, 0, st>>>(
-        A, a.B, a.ws, a.gscale, a.fscale, bias, Y, a.M, a.N, a.K, a.bs);
+        A, a.B, a.ws, a.gscale, a.fscale, a.ascale, bias, Y, a.M, a.N, a.K, a.bs);
   else
     gemv_general<DT, KIND, false><<<grid, kGemvWarps * 32, 0, st>>>(
-        A, a.B, a.ws, a.gscale, a.fscale, bias, Y, a.M, a.N, a.K, a.bs);
+        A, a.B, a.ws, a.gscale, a.fscale, a.ascale, bias, Y, a.M, a.N, a.K, a.bs);
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 
@@ -375,6 +381,7 @@ struct FastParams {
   const uint8_t* ws;      // NVFP4 scales
   const float* gscale;
   const float* fscale;    // FP8 scales
+  const float* ascale;    // FP8 W8A8 activation scale, or nullptr
   const uint16_t* bias;
   uint16_t* Y;
   int M, N, K;
@@ -584,6 +591,12 @@ __global__ void __launch_bounds__(kFastWarps * 32, 2) gemv_fast(const FastParams
       const int k = k_lo + cv * 8;
       uint4 val = make_uint4(0, 0, 0, 0);
       if (k < p.K) val = __ldg(reinterpret_cast<const uint4*>(p.A + (int64_t)m * p.K + k));
+      if (p.ascale != nullptr) {
+        // W8A8: the activation is quantized and dequantized as it is staged.
+        const float a_s = __ldg(p.ascale);
+        val = make_uint4(qdq_fp8_act_pair<DT>(val.x, a_s), qdq_fp8_act_pair<DT>(val.y, a_s),
+                         qdq_fp8_act_pair<DT>(val.z, a_s), qdq_fp8_act_pair<DT>(val.w, a_s));
+      }
       *reinterpret_cast<uint4*>(act + m * p.act_pitch + cv * 16) = val;
     }
   }
@@ -678,6 +691,7 @@ int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
   p.ws = a.ws;
   p.gscale = a.gscale;
   p.fscale = a.fscale;
+  p.ascale = a.ascale;
   p.bias = reinterpret_cast<const uint16_t*>(a.bias);
   p.Y = reinterpret_cast<uint16_t*>(a.Y);
   p.M = (int)a.M;
@@ -1144,6 +1158,39 @@ int launch_tma_dt(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
 }
 
 }  // namespace
+
+// Standalone W8A8 activation quantize-dequantize: eight elements per thread
+// (16-byte loads and stores), the tail element by element.
+template <int DT>
+__global__ void fp8_qdq_act_kernel(const uint16_t* __restrict__ A, const float* __restrict__ ascale,
+                                   uint16_t* __restrict__ out, int64_t n) {
+  const float a_s = __ldg(ascale);
+  const int64_t n8 = n / 8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(A) + i);
+    reinterpret_cast<uint4*>(out)[i] =
+        make_uint4(qdq_fp8_act_pair<DT>(v.x, a_s), qdq_fp8_act_pair<DT>(v.y, a_s),
+                   qdq_fp8_act_pair<DT>(v.z, a_s), qdq_fp8_act_pair<DT>(v.w, a_s));
+  }
+  const int64_t tail = n8 * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tail < n) out[tail] = (uint16_t)(qdq_fp8_act_pair<DT>(A[tail], a_s) & 0xFFFFu);
+}
+
+int launch_fp8_qdq_activation(const void* A, const float* a_scale, void* out, int64_t n,
+                              int dtype, cudaStream_t st) {
+  if (n == 0) return kOk;
+  const DeviceInfo& d = device_info();
+  const int64_t blocks = std::min<int64_t>(std::max<int64_t>((n / 8 + 255) / 256, 1),
+                                           (int64_t)d.sm_count * 8);
+  auto a = reinterpret_cast<const uint16_t*>(A);
+  auto o = reinterpret_cast<uint16_t*>(out);
+  if (dtype == 1)
+    fp8_qdq_act_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(a, a_scale, o, n);
+  else
+    fp8_qdq_act_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(a, a_scale, o, n);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
 
 bool gemv_tma_supports(const GemvArgs& a) {
   TmaPlan tp;

@@ -60,6 +60,7 @@ struct GemvArgs {
   const uint8_t* ws;      // NVFP4 block scales [N, S]
   const float* gscale;    // NVFP4 weight_scale_2 (device)
   const float* fscale;    // FP8 block scales [N, S]
+  const float* ascale;    // FP8 W8A8: activation scale (device), or nullptr
   const void* bias;
   void* Y;
   int64_t M, N, K;
@@ -69,6 +70,10 @@ struct GemvArgs {
 int launch_gemv(const GemvArgs& a, cudaStream_t st);
 // The TMA decode GEMV also takes 8 < M <= 32 (NVFP4, bs 16, K % 256 == 0).
 bool gemv_tma_supports(const GemvArgs& a);
+
+// W8A8 activation quantize-dequantize over n elements (wqmm_gemv.cu).
+int launch_fp8_qdq_activation(const void* A, const float* a_scale, void* out, int64_t n,
+                              int dtype, cudaStream_t st);
 
 // ---- fused tcgen05 GEMM for large M (wqmm_gemm.cu) ----
 // Returns kUnsupported if the shape cannot take this path.

@@ -105,6 +105,39 @@ int fp8_weight_matmul(const void* A, const uint8_t* B, const float* b_scale,
                       int block_size, int dtype, void* stream);
 
 /*
+ * fp8_weight_matmul_w8a8 -- the optional W8A8 activation path of the FP8
+ * operator: Y = A_deq * dequant(B)^T (+ bias) with
+ * [FP8] §6 Optional W8A8 Activation Path:
+ *     A_deq = fp8_e4m3(A / a_scale) * a_scale
+ * computed inside the GEMV's activation loads (no [M, K] scratch).
+ *
+ *   a_scale  device pointer to one float32 (the static activation scale).
+ *   Other arguments, layouts and errors as for fp8_weight_matmul; a NULL
+ *   a_scale (with a non-empty output) is INVALID_ARG.
+ * Per element: one float32 division (IEEE), E4M3FN by round-to-nearest-even
+ * saturating at +-448 (NaN stays NaN), one float32 multiplication by a_scale,
+ * one RNE to dtype; exactly fp8_quantize_dequantize_activation.
+ * Paths: the decode GEMV for every M (per 8-row group above 8 rows, each
+ * group streaming the whole weight); for prefill-sized M the cheaper route
+ * is fp8_quantize_dequantize_activation into a caller-owned [M, K] buffer
+ * followed by fp8_weight_matmul, which gives the same A_deq bit for bit.
+ * Accuracy: the bound of fp8_weight_matmul with A_deq in place of A.
+ */
+int fp8_weight_matmul_w8a8(const void* A, const float* a_scale, const uint8_t* B,
+                           const float* b_scale, const void* bias, void* Y, int64_t M,
+                           int64_t N, int64_t K, int block_size, int dtype, void* stream);
+
+/*
+ * fp8_quantize_dequantize_activation -- out = A_deq as defined above, for
+ * `count` activation elements (any shape, contiguous).  Bit-exact contract.
+ *   A, out   count values of dtype (16-byte aligned, may not overlap partly).
+ *   a_scale  device pointer to one float32.
+ * Errors: count < 0 or a NULL pointer with count > 0 -> INVALID_ARG.
+ */
+int fp8_quantize_dequantize_activation(const void* A, const float* a_scale, void* out,
+                                       int64_t count, int dtype, void* stream);
+
+/*
  * fp4_dequantize -- expand an NVFP4 weight to the activation type.
  * [FP4] §2 formula, §5 step 1; [BLOG] vectorised dequant.
  *   out[n, k] = RNE_dtype( fp32( fp32(e2m1 * e4m3) * weight_scale_2 ) )

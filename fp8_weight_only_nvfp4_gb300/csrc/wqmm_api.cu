@@ -10,7 +10,8 @@
 //   K == 0                -> Y = bias (or 0)
 //   M <= 8                -> decode GEMV
 //   M <= 32, NVFP4 bs 16, K % 256 == 0 -> decode GEMV (up to four 8-row tiles)
-//   M > 8, GEMM-eligible  -> fused tcgen05 GEMM (weight decoded in the main loop)
+//   M > 8, GEMM-eligible  -> fused tcgen05 GEMM (weight decoded in the main loop;
+//                            token tile 32 / 64 / 128 / 256 by M)
 //   otherwise             -> decode GEMV, one launch per 8-row group
 #include <mutex>
 #include <cstring>

@@ -11,11 +11,13 @@
 // the packed weight is decoded inside the GEMM main loop, straight into
 // tensor memory, and never written back to global memory.
 //
-// Tile: 128 weight rows (MMA M) x 256 tokens (MMA N) per CTA, K in stages of
-// 64.  Roles (one CTA = 18 warps):
-//   warp 0     TMA producer: activation tile [256 tokens x 64 k] (128-byte
+// Tile: 128 weight rows (MMA M) x BN tokens (MMA N) per CTA, K in stages of
+// 64; BN = 256 for prefill, 128 / 64 / 32 when M fits a narrower tile.
+// Roles (one CTA = 18 warps):
+//   warp 0     TMA producer: activation tile [BN tokens x 64 k] (128-byte
 //              swizzle, K-major) and packed weight tile [128 rows x 64 k]
-//              into a shared-memory ring (6 stages for NVFP4, 5 for FP8);
+//              into a shared-memory ring (6 stages for NVFP4 and 5 for FP8
+//              at BN = 256, up to 12 for narrower tiles);
 //   warp 1     TMEM owner and MMA issuer (one elected thread):
 //              tcgen05.mma.kind::f16, A = decoded weight from TMEM,
 //              B = activation tile from shared memory, D = FP32 in TMEM;
@@ -25,7 +27,7 @@
 //              shared memory, folds the E4M3 block scales (exact for NVFP4:
 //              <= 6 significant bits, FP4 page §4), writes the 16-bit
 //              operands to TMEM with one tcgen05.st, and after the main loop
-//              runs the epilogue for a quarter of the 256 token columns: TMEM
+//              runs the epilogue for a quarter of the BN token columns: TMEM
 //              -> registers, * gscale, + bias, one RNE, then Y (through a
 //              shared-memory transpose and one tensor store when the row
 //              pitch allows, else direct stores with lanes = consecutive n).
@@ -57,24 +59,31 @@ namespace wqmm {
 namespace {
 
 constexpr int kBM = 128;       // weight rows per tile (MMA M)
-constexpr int kBN = 256;       // tokens per tile (MMA N)
 constexpr int kBK = 64;        // k per stage
 constexpr int kDecWarps = 16;  // four per TMEM lane quarter, taking the stages in turn
 constexpr int kThreads = (2 + kDecWarps) * 32;
-constexpr int kActStageBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kTmemCols = 512;
-constexpr int kAccCol = 0;                      // accumulator: columns [0, 256)
-constexpr int kACol = 256;                      // A stages: columns [256, 256 + 32 * stages)
+constexpr int kAccCol = 0;     // accumulator: columns [0, BN)
 
-// Ring depth per weight format: as many stages as shared memory holds (the
-// ring has to cover the tensor-copy latency; a stage is 32 KB of activation
-// plus the packed weight tile, 4 KB for NVFP4 and 8 KB for FP8).
-template <int KIND>
+// Layout per weight format (KIND 0 = NVFP4, 1 = FP8) and token-tile width BN
+// (the MMA N: 256 for prefill, 128 / 64 / 32 for mid-range M, where a
+// 256-token tile would spend most of its MMA work on padding rows).  The
+// ring holds as many stages as shared memory and tensor memory allow (it has
+// to cover the tensor-copy latency): a stage is the activation tile [BN x 64
+// k] plus the packed weight tile (4 KB NVFP4, 8 KB FP8) in shared memory and
+// 32 tensor-memory columns of decoded operand.
+template <int KIND, int BN>
 struct GemmCfg {
-  static constexpr int stages = KIND == 0 ? 6 : 5;
+  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "token tile");
+  static constexpr int act_stage = BN * kBK * 2;
   static constexpr int wstage = KIND == 0 ? kBM * kBK / 2 : kBM * kBK;
+  static constexpr int a_col = BN;                         // A stages after the accumulator
+  static constexpr int tmem_stages = (kTmemCols - a_col) / (kBK / 2);
+  static constexpr int smem_stages = (216 * 1024) / (act_stage + wstage);
+  static constexpr int stages0 = tmem_stages < smem_stages ? tmem_stages : smem_stages;
+  static constexpr int stages = stages0 > 12 ? 12 : stages0;
   static constexpr int act = 0;
-  static constexpr int w = act + stages * kActStageBytes;
+  static constexpr int w = act + stages * act_stage;
   static constexpr int bars = w + stages * wstage;
   static constexpr int full = bars;
   static constexpr int empty = full + 8 * stages;
@@ -84,8 +93,14 @@ struct GemmCfg {
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int total = abort_flag + 4;
   static constexpr int smem_bytes = total + 1024;  // + alignment slack
-  static_assert(kACol + stages * (kBK / 2) <= kTmemCols, "TMEM columns");
+  static_assert(stages >= 4, "ring depth");
+  static_assert(a_col + stages * (kBK / 2) <= kTmemCols, "TMEM columns");
   static_assert(smem_bytes <= 227 * 1024, "shared memory");
+  // The Y staging tile [BN x 128] and the split-K receive slots (at most 3 x
+  // BN/4 columns x 128 rows of FP32, rounded up to 8 columns) fit in the
+  // activation ring.
+  static_assert(BN * kBM * 2 <= stages * act_stage, "Y staging");
+  static_assert(3 * ((BN / 4 + 7) / 8 * 8) * kBM * 4 <= stages * act_stage, "split-K slots");
 };
 
 // ---------------------------------------------------------------------------
@@ -179,6 +194,18 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -187,6 +214,15 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
       : "r"(taddr)
       : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Loads N = 8, 16 or 32 consecutive accumulator columns of this warp's lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[N]) {
+  static_assert(N == 8 || N == 16 || N == 32, "column count");
+  if constexpr (N == 32) tmem_ld32(taddr, v);
+  else if constexpr (N == 16) tmem_ld16(taddr, v);
+  else tmem_ld8(taddr, v);
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
@@ -202,10 +238,11 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {
 }
 
 // Instruction descriptor, kind::f16: D = F32, A/B = F16 (0) or BF16 (1),
-// both K-major, N = 256, M = 128.
+// both K-major, N = BN, M = 128.
+template <int BN>
 __host__ __device__ constexpr uint32_t make_idesc(int ab_fmt) {
   return (1u << 4) | ((uint32_t)ab_fmt << 7) | ((uint32_t)ab_fmt << 10) |
-         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
 // Bounded wait that also gives up as soon as another role raised the abort flag.
@@ -256,15 +293,16 @@ __device__ __forceinline__ void decode_fp4_word(uint32_t w, uint32_t sc16, uint3
   for (int i = 0; i < 4; ++i) out[i] = fold_f16x2<DT>(h[i], sc2);
 }
 
-// KIND 0 = NVFP4 weight, 1 = FP8 weight.  DT 0 = FP16, 1 = BF16.
-template <int DT, int KIND>
+// KIND 0 = NVFP4 weight, 1 = FP8 weight.  DT 0 = FP16, 1 = BF16.  BN =
+// tokens per tile (MMA N).
+template <int DT, int KIND, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmY, int y_tma,
                    const uint8_t* __restrict__ ws, const float* __restrict__ gscale,
                    const float* __restrict__ fscale, const uint16_t* __restrict__ bias,
                    uint16_t* __restrict__ Y, int M, int N, int K, int bs, int* err) {
-  using L = GemmCfg<KIND>;
+  using L = GemmCfg<KIND, BN>;
   constexpr int kStages = L::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -279,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBM;
-  const int m0 = blockIdx.y * kBN;
+  const int m0 = blockIdx.y * BN;
   const int num_k_all = (K + kBK - 1) / kBK;
   // Split-K across a cluster of C CTAs along gridDim.z: rank r takes stages
   // [k_lo, k_lo + num_k) (the host sizes ranks so that every one has some).
@@ -315,13 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint32_t bytes = kActStageBytes + kBM * kWBytes;
+      const uint32_t bytes = L::act_stage + kBM * kWBytes;
       int issued = 0;
       for (int it = 0; it < num_k; ++it) {
         const int s = it % kStages;
         if (it >= kStages && !wait_bar(&empty[s], ((it / kStages) + 1) & 1, err, abort_flag)) break;
         mbar_arrive_expect_tx(&full[s], bytes);
-        tma_load_2d(smem + L::act + s * kActStageBytes, &tmA, (k_lo + it) * kBK, m0, &full[s]);
+        tma_load_2d(smem + L::act + s * L::act_stage, &tmA, (k_lo + it) * kBK, m0, &full[s]);
         tma_load_2d(smem + L::w + s * L::wstage, &tmW, (k_lo + it) * kWBytes, n0, &full[s]);
         ++issued;
       }
@@ -334,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(DT == 1 ? 1 : 0);
+      constexpr uint32_t idesc = make_idesc<BN>(DT == 1 ? 1 : 0);
       bool ok = true;
       int committed = -1;
       for (int it = 0; it < num_k && ok; ++it) {
@@ -343,11 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_bar(&full[s], par, err, abort_flag) && wait_bar(&afull[s], par, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t act_addr = smem_u32(smem + L::act + s * kActStageBytes);
+        const uint32_t act_addr = smem_u32(smem + L::act + s * L::act_stage);
         const uint64_t bdesc = desc_kmajor_sw128(act_addr);
 #pragma unroll
         for (int j = 0; j < kBK / 16; ++j) {
-          const uint32_t a_tmem = tmem + kACol + s * (kBK / 2) + j * 8;
+          const uint32_t a_tmem = tmem + L::a_col + s * (kBK / 2) + j * 8;
           mma_ts(tmem + kAccCol, a_tmem, bdesc + (uint64_t)((j * 32) >> 4), idesc,
                  (it > 0 || j > 0) ? 1u : 0u);
         }
@@ -439,14 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tmem_st32(lane_base + kACol + s * (kBK / 2), v);
+      tmem_st32(lane_base + L::a_col + s * (kBK / 2), v);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[s]);  // one arrival per lane quarter
     }
-    // Epilogue: this warp's lane quarter, token columns [64 j4, 64 j4 + 64).
-    // With a tensor map for Y the tile is staged transposed, [256 tokens x
+    // Epilogue: this warp's lane quarter, token columns [BN/4 j4, BN/4 (j4 + 1)).
+    // With a tensor map for Y the tile is staged transposed, [BN tokens x
     // 128 n], in the (now idle) activation ring and written by one tensor
     // store; otherwise each column is stored directly (lanes = consecutive n).
     have = ok && wait_bar(accfull, 0, err, abort_flag);
@@ -455,17 +493,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
       uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + L::act);
+      constexpr int kCW = BN / 4;                    // columns of this warp
+      constexpr int kCh = kCW < 32 ? kCW : 32;       // columns per tensor-memory load
 #pragma unroll 1
-      for (int c0 = 64 * j4; c0 < 64 * j4 + 64; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + kAccCol + c0, r);
+      for (int c0 = kCW * j4; c0 < kCW * j4 + kCW; c0 += kCh) {
+        uint32_t r[kCh];
+        tmem_ld_cols<kCh>(lane_base + kAccCol + c0, r);
         if (y_tma) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < kCh; ++j)
             stage_y[(c0 + j) * kBM + row] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
         } else if (n < N) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < kCh; ++j) {
             const int m = m0 + c0 + j;
             if (m < M) Y[(int64_t)m * N + n] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
           }
@@ -490,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Split-K: reduce-scatter of the FP32 partial tiles through distributed
-  // shared memory.  Token columns are cut into C blocks (multiples of 32);
+  // shared memory.  Token columns are cut into C blocks (multiples of 8);
   // rank b owns block b: every other rank writes its partial of that block
   // into rank b's (now idle) activation ring, then rank b adds them in rank
   // order to its own and runs the epilogue for the block.  Deterministic, no
@@ -498,8 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (C > 1) {
     __syncwarp();
     cluster_sync();  // every rank's MMAs are complete and its rings are idle
-    const int wmax = (kBN / C + 31) / 32 * 32;
-    auto block_lo = [&](int bb) { return min(kBN, bb * wmax); };
+    const int wmax = (BN / C + 7) / 8 * 8;
+    auto block_lo = [&](int bb) { return min(BN, bb * wmax); };
     // [C-1 slots][wmax columns][128 rows]: lanes (consecutive rows) write and
     // read consecutive words, one 128-byte line per warp access.
     float* recv = reinterpret_cast<float*>(smem + L::act);
@@ -512,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bb == rank) continue;
         const int c_lo = block_lo(bb), w = block_lo(bb + 1) - c_lo;
         const int slot = rank < bb ? rank : rank - 1;
-        // This warp: columns [w/4 * j4, w/4 * (j4 + 1)) of the block, 8 at a time.
-        for (int c8 = (w / 4) * j4; c8 < (w / 4) * (j4 + 1); c8 += 8) {
+        // This warp: the block's 8-column chunks j4, j4 + 4, ...
+        for (int c8 = 8 * j4; c8 < w; c8 += 32) {
           uint32_t r[8];
           tmem_ld8(lane_base + kAccCol + c_lo + c8, r);
           const uint32_t remote =
@@ -533,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float bv = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
       const int c_lo = block_lo(rank), w = block_lo(rank + 1) - c_lo;
-      for (int c8 = (w / 4) * j4; c8 < (w / 4) * (j4 + 1); c8 += 8) {
+      for (int c8 = 8 * j4; c8 < w; c8 += 32) {
         uint32_t r[8];
         tmem_ld8(lane_base + kAccCol + c_lo + c8, r);
         // Rank order: partials of ranks 0 .. C-1, this rank's own in place.
@@ -572,13 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DT, int KIND>
+template <int DT, int KIND, int BN>
 int launch_t(const GemvArgs& a, cudaStream_t st) {
   const int wbytes_per_stage = (KIND == 0) ? kBK / 2 : kBK;
   CUtensorMap tmA, tmW;
   const CUtensorMapDataType adt =
       DT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (!encode_tmap_2d(&tmA, adt, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, kBK, kBN,
+  if (!encode_tmap_2d(&tmA, adt, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, kBK, BN,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return kCuda;
   const uint64_t wrow = (KIND == 0) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
@@ -593,17 +633,21 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
   std::memset(&tmY, 0, sizeof(tmY));
   if (a.N % 8 == 0)
     y_tma = encode_tmap_2d(&tmY, adt, a.Y, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.N * 2, kBM,
-                           kBN, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
+                           BN, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
                 ? 1
                 : 0;
-  static std::once_flag once[2][2];
-  std::call_once(once[DT][KIND], [] {
-    cudaFuncSetAttribute(gemm_tc_kernel<DT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         GemmCfg<KIND>::smem_bytes);
+  using L = GemmCfg<KIND, BN>;
+  // The shared-memory opt-in is a per-device function attribute.
+  static std::once_flag once[64];
+  const int dev = device_info().device;
+  if (dev < 0 || dev >= 64) return kCuda;
+  std::call_once(once[dev], [] {
+    cudaFuncSetAttribute(gemm_tc_kernel<DT, KIND, BN>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
   });
   // Split-K (cluster of C CTAs along z) when the tiles fill less than half
   // of the GPU: each rank decodes and multiplies 1/C of K, one CTA per SM.
-  const int64_t tiles_n = (a.N + kBM - 1) / kBM, tiles_m = (a.M + kBN - 1) / kBN;
+  const int64_t tiles_n = (a.N + kBM - 1) / kBM, tiles_m = (a.M + BN - 1) / BN;
   const int64_t tiles = tiles_n * tiles_m;
   const int num_k = (int)((a.K + kBK - 1) / kBK);
   const int sms = device_info().sm_count;
@@ -619,12 +663,14 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
       const int spc = (num_k + C - 1) / C;
       C = (num_k + spc - 1) / spc;
     }
+    // The receive slots of the reduce-scatter live in the activation ring.
+    while (C > 1 && (C - 1) * ((BN / C + 7) / 8 * 8) * kBM * 4 > L::stages * L::act_stage) --C;
   }
   const dim3 grid((unsigned)tiles_n, (unsigned)tiles_m, (unsigned)C);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = GemmCfg<KIND>::smem_bytes;
+  cfg.dynamicSmemBytes = L::smem_bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -634,10 +680,30 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, gemm_tc_kernel<DT, KIND>, tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale,
+      &cfg, gemm_tc_kernel<DT, KIND, BN>, tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale,
       reinterpret_cast<const uint16_t*>(a.bias), reinterpret_cast<uint16_t*>(a.Y), (int)a.M,
       (int)a.N, (int)a.K, a.bs, device_error_word());
   return e == cudaSuccess ? kOk : kCuda;
+}
+
+// Token-tile width by M: the narrowest MMA N that covers M in one tile up to
+// 128 tokens (a wider tile multiplies padding rows), 256 above that (one
+// decode of the weight tile feeds the most tokens).
+int pick_bn(int64_t M) {
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+template <int DT, int KIND>
+int launch_bn(const GemvArgs& a, cudaStream_t st) {
+  switch (pick_bn(a.M)) {
+    case 32: return launch_t<DT, KIND, 32>(a, st);
+    case 64: return launch_t<DT, KIND, 64>(a, st);
+    case 128: return launch_t<DT, KIND, 128>(a, st);
+    default: return launch_t<DT, KIND, 256>(a, st);
+  }
 }
 
 }  // namespace
@@ -645,8 +711,10 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
 bool gemm_supports(const GemvArgs& a) {
   const DeviceInfo& d = device_info();
   if (d.cc_major != 10) return false;
-  if (d.max_smem_optin < (a.kind == 0 ? GemmCfg<0>::smem_bytes : GemmCfg<1>::smem_bytes))
-    return false;
+  constexpr int kMaxSmem = GemmCfg<1, 256>::smem_bytes > GemmCfg<1, 128>::smem_bytes
+                               ? GemmCfg<1, 256>::smem_bytes
+                               : GemmCfg<1, 128>::smem_bytes;
+  if (d.max_smem_optin < kMaxSmem) return false;
   if (a.M <= 8 || a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31)) return false;
   if (a.bs % 16 != 0) return false;
   if (a.kind == 0) return a.K % 32 == 0;   // packed row stride must be a multiple of 16 bytes
@@ -656,8 +724,8 @@ bool gemm_supports(const GemvArgs& a) {
 int launch_gemm(const GemvArgs& a, cudaStream_t st) {
   if (!gemm_supports(a)) return kUnsupported;
   if (a.kind == 0)
-    return a.dtype == 1 ? launch_t<1, 0>(a, st) : launch_t<0, 0>(a, st);
-  return a.dtype == 1 ? launch_t<1, 1>(a, st) : launch_t<0, 1>(a, st);
+    return a.dtype == 1 ? launch_bn<1, 0>(a, st) : launch_bn<0, 0>(a, st);
+  return a.dtype == 1 ? launch_bn<1, 1>(a, st) : launch_bn<0, 1>(a, st);
 }
 
 }  // namespace wqmm

@@ -25,10 +25,13 @@ def test_small_shapes(M, N, K, bs, dtype):
     assert_within_tolerance(run_fp4(p), *_ref(p), dtype, f"gemm {M}x{N}x{K} bs={bs}")
 
 
-def test_one_hot_probe_gemm():
+@pytest.mark.parametrize("M", [24, 64, 128, 256])
+def test_one_hot_probe_gemm(M):
     """Bit-exact one-hot probe through the GEMM path (weight_scale_2 = 1, no
-    bias): token m selects column k(m) of the weight; Y[m, n] = B_dq[n, k(m)]."""
-    M, N, K, bs = 256, 128, 256, 16
+    bias): token m selects column k(m) of the weight; Y[m, n] = B_dq[n, k(m)].
+    M = 24 / 64 / 128 / 256 run the 32 / 64 / 128 / 256-token tiles (K = 320
+    keeps M = 24 off the decode GEMV)."""
+    N, K, bs = 128, 320, 16
     p = wl.make_fp4(M, N, K, bs, oracle.BF16, seed=17, ws2=1.0)
     d = fp4_dev(p)
     W = oracle.fp4_dequantize_f64(p.B_packed, p.weight_scale, 1.0, N, K, bs)
@@ -142,3 +145,40 @@ def test_fp8_split_k():
     Y = run_fp8(p)
     Yr, S = oracle.fp8_matmul(p.A, p.B, p.b_scale, p.bias, p.M, p.N, p.K, p.block_size, p.dtype)
     assert_within_tolerance(Y, Yr, S, p.dtype, "fp8 split-K")
+
+
+# --- mid-range M: the token tile narrows to 32 / 64 / 128 (MMA N) so that a
+# --- small batch does not pay for a 256-token tile of padding rows
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+@pytest.mark.parametrize("M,N,K,bs", [
+    (24, 256, 320, 16),     # 32-token tile (K % 256 != 0 keeps it off the GEMV)
+    (32, 384, 640, 32),     # 32-token tile, bs 32
+    (20, 256, 4160, 16),    # 32-token tile, split-K over 4 ranks (K % 256 != 0)
+    (48, 200, 512, 16),     # 64-token tile, ragged N
+    (64, 128, 1024, 16),    # 64-token tile, full
+    (40, 640, 2048, 16),    # 64-token tile, split-K (5 tiles, 4 ranks)
+    (65, 256, 256, 16),     # 128-token tile, one real row past the 64-token tile
+    (128, 129, 768, 16),    # 128-token tile, full, ragged N
+    (100, 1280, 1600, 16),  # 128-token tile, split-K (10 tiles, 3 ranks)
+    (129, 64, 320, 16),     # back to the 256-token tile
+])
+def test_mid_m_tiles(M, N, K, bs, dtype):
+    p = wl.make_fp4(M, N, K, bs, dtype, seed=M * 7 + N + K, bias_sigma=0.05)
+    assert_within_tolerance(run_fp4(p), *_ref(p), dtype, f"mid-M {M}x{N}x{K} bs={bs}")
+
+
+@pytest.mark.parametrize("M,N,K,bs", [(20, 256, 4096, 128), (33, 300, 1024, 64),
+                                      (96, 257, 1024, 128), (128, 64, 5120, 128)])
+def test_fp8_mid_m_tiles(M, N, K, bs):
+    p = wl.make_fp8(M, N, K, bs, oracle.BF16, seed=M + K, bias_sigma=0.05)
+    Yr, S = oracle.fp8_matmul(p.A, p.B, p.b_scale, p.bias, M, N, K, bs, p.dtype)
+    assert_within_tolerance(run_fp8(p), Yr, S, p.dtype, f"fp8 mid-M {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [64, 128])
+def test_mid_m_gate_up_sampled(M):
+    """M = 64 / 128 tokens at the gate/up shape (N = 17408, K = 5120), as the
+    benchmark times it: sampled outputs plus full rows and columns."""
+    p = wl.make_fp4(M, 17408, 5120, 16, oracle.BF16, seed=M, bias_sigma=0.02)
+    _sampled_check(p, run_fp4, _fp4_sampled, n_random=2048)

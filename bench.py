@@ -398,6 +398,28 @@ def bench_also(gpu, args, peaks):
         out[f"gemv_M{M}_N5120_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
                                          "us_per_layer": round(dt / (reps * LAYERS) * 1e6, 2)}
         del g
+    # Mid-range M (fused GEMM with a 64- or 128-token tile): R launches over
+    # distinct weights per graph (more than L2 in total), TFLOP/s and weight
+    # GB/s per launch.
+    for (N, K, R) in ((17408, 5120, 4), (5120, 5120, 12)):
+        lys = gpu.fp4_layers(8, N, K, R, seed0=800)
+        for M in (64, 128):
+            A = torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16)
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+
+            def midm_step():
+                for ly in lys:
+                    wq.fp4_weight_matmul(A, ly["B"], ly["ws"], ly["ws2"], None, 16, out=Y,
+                                         stream=gpu.stream)
+            g = gpu.graph(midm_step)
+            reps = max(5, args.steps // 5)
+            dt = gpu.time_graph(g, reps, 2) / (reps * R)
+            tf = 2 * M * N * K / dt / 1e12
+            out[f"gemm_M{M}_N{N}_K{K}"] = {"TFLOP/s": round(tf, 1), "frac": round(tf / tf_peak, 4),
+                                           "GB/s": round(gemv_bytes(M, N, K) / dt / 1e9, 1),
+                                           "us": round(dt * 1e6, 2)}
+            del g
+        del lys
     # Whole decode step: one CUDA graph of 120 weight-only GEMVs shaped like a
     # 27B-class decoder (hidden 5120, MLP 17408): per layer four 5120 x 5120
     # projections, gate and up 17408 x 5120, down 5120 x 17408 (17 layers), then

@@ -371,9 +371,23 @@ def bench_also(gpu, args, peaks):
             dq = lambda: wq.fp4_dequantize(ly["B"], ly["ws"], ly["ws2"], 16, out=W,
                                            stream=gpu.stream)
             dt_dq = gpu.time_each(dq, reps=5, warmup=2)
-            gbs = dequant_bytes(N, K) / dt_dq / 1e9
+            # Standalone dequantize: a graph of R launches over R distinct
+            # weights and outputs (912 MB in total, far above L2), per launch.
+            R = 4
+            dls = gpu.fp4_layers(1, N, K, R, seed0=720)
+            Ws = [torch.empty(N, K, dtype=torch.bfloat16, device=gpu.dev) for _ in range(R)]
+
+            def dq_step():
+                for d, w in zip(dls, Ws):
+                    wq.fp4_dequantize(d["B"], d["ws"], d["ws2"], 16, out=w, stream=gpu.stream)
+            gq = gpu.graph(dq_step)
+            reps = max(5, args.steps // 5)
+            dt_g = gpu.time_graph(gq, reps, 2) / (reps * R)
+            gbs = dequant_bytes(N, K) / dt_g / 1e9
             out[f"dequant_N{N}_K{K}"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
-                                         "us": round(dt_dq * 1e6, 2)}
+                                         "us": round(dt_g * 1e6, 2),
+                                         "us_single_launch_l2_flushed": round(dt_dq * 1e6, 2)}
+            del gq, dls, Ws
             mm = lambda: torch.matmul(A, W.t())
             with torch.cuda.stream(gpu.stream):
                 dt_mm = gpu.time_each(mm, reps=5, warmup=2)

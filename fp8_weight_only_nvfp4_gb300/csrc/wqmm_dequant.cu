@@ -16,6 +16,8 @@
 //    so every load instruction reads 128 contiguous bytes per warp (NVFP4) and
 //    every store instruction writes 512 contiguous bytes per warp.
 //  * All U loads are issued before any conversion (memory-level parallelism).
+//  * The output is written with streaming (evict-first) stores: it is written
+//    once and, for the weights the pages dequantize, larger than L2.
 //  * weight_scale_2 is read once per thread into a register.
 //  * E2M1 and E4M3 decode with the hardware cvt instructions (exact); the two
 //    multiplies use __fmul_rn so that no FMA contraction changes the rounding.
@@ -67,7 +69,7 @@ __global__ void __launch_bounds__(kThreads)
         const float t1 = __fmul_rn(__fmul_rn(c.y, sc), ws2);
         o[i] = pack2_rn<DT>(t0, t1);
       }
-      stg_v4(out + u, make_uint4(o[0], o[1], o[2], o[3]));
+      stg_v4_stream(out + u, make_uint4(o[0], o[1], o[2], o[3]));
     }
   }
 }
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kThreads)
         const float2 c = f16x2_to_f32x2(e4m3x2_to_f16x2(two));
         o[i] = pack2_rn<DT>(__fmul_rn(c.x, sc[j]), __fmul_rn(c.y, sc[j]));
       }
-      stg_v4(out + u, make_uint4(o[0], o[1], o[2], o[3]));
+      stg_v4_stream(out + u, make_uint4(o[0], o[1], o[2], o[3]));
     }
   }
 }

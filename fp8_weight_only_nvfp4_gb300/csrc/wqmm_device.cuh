@@ -227,6 +227,14 @@ __device__ __forceinline__ void stg_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// 16-byte streaming store (evict-first): for outputs written once and larger
+// than L2.
+__device__ __forceinline__ void stg_v4_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Format decoders
 // ---------------------------------------------------------------------------

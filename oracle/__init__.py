@@ -17,7 +17,11 @@ Function map (all cite the pages by title and section):
 * ``fp4_matmul`` / ``fp8_matmul`` (+ ``*_sampled``) -- the operator definition
   Y = A * dequant(B)^T + bias, exact decode in float64 and float64 sums, plus
   the magnitude sum S = sum_k |A[m,k] * B_dq[n,k]| used by the tolerance.
-* ``e2m1_value``, ``e4m3_value``, ``rne_f32_to_act`` -- the format primitives.
+* ``nvfp4_quantize_activation`` / ``nvfp4_qdq_activation`` -- "MatMulBlockQuantizedFp4Weight"
+  §6 step 1 (NVFP4 activation quantization, per-16 E4M3 scales).
+* ``fp8_qdq_activation`` -- "MatMulBlockQuantizedFp8Weight" §6 (W8A8).
+* ``e2m1_value``, ``e4m3_value``, ``e2m1_from_f32``, ``e4m3_from_f32``,
+  ``rne_f32_to_act`` -- the format primitives.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against values the
 pages print, library routines (torch float8_e4m3fn and dtype casts), closed
@@ -88,6 +92,10 @@ def _load():
         lib.orc_e4m3_from_f32.argtypes = [F]
         lib.orc_e4m3_from_f32.restype = I
         lib.orc_fp8_qdq_activation.argtypes = [P, F, P, I64, I]
+        lib.orc_e2m1_from_f32.argtypes = [F]
+        lib.orc_e2m1_from_f32.restype = I
+        lib.orc_nvfp4_quantize_act.argtypes = [P, I64, I64, I, P, P]
+        lib.orc_nvfp4_qdq_act.argtypes = [P, I64, I64, I, P]
         _lib = lib
         return lib
 
@@ -128,6 +136,36 @@ def fp8_qdq_activation(A, a_scale: float, dtype: int) -> np.ndarray:
     out = np.empty(a.shape, dtype=np.uint16)
     _load().orc_fp8_qdq_activation(_ptr(a), float(np.float32(a_scale)), _ptr(out), a.size,
                                    int(dtype))
+    return out
+
+
+def e2m1_from_f32(f: float) -> int:
+    """E2M1 code of a float32 value: RNE, ties to even, saturating at 6, sign
+    kept (a negative value that rounds to zero gives 0x8)."""
+    return int(_load().orc_e2m1_from_f32(float(np.float32(f))))
+
+
+def nvfp4_quantize_activation(A, dtype: int):
+    """NVFP4 activation quantization (FP4 page §6, step 1 of the native
+    path): per 16-element block of each row, scale = E4M3(fp32(amax / 6)),
+    codes = E2M1(fp32(a / scale)).  A is [M, K] activation bit patterns (K
+    even); returns (codes [M, K/2] uint8, two per byte with the even k in the
+    low nibble; scales [M, ceil(K/16)] uint8)."""
+    a = _c(A, np.uint16)
+    M, K = a.shape
+    codes = np.empty((M, K // 2), dtype=np.uint8)
+    scales = np.empty((M, (K + 15) // 16), dtype=np.uint8)
+    _load().orc_nvfp4_quantize_act(_ptr(a), M, K, int(dtype), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def nvfp4_qdq_activation(A, dtype: int) -> np.ndarray:
+    """NVFP4 activation quantize-dequantize: RNE_act(e2m1(code) * e4m3(scale))
+    per element (exact: at most 6 significant bits); same shape as A."""
+    a = _c(A, np.uint16)
+    M, K = a.shape
+    out = np.empty_like(a)
+    _load().orc_nvfp4_qdq_act(_ptr(a), M, K, int(dtype), _ptr(out))
     return out
 
 

@@ -25,6 +25,10 @@
 //   * matmul reference: exact decode in float64, float64 sums, bias added in
 //     float64; the tolerance is applied by the caller.
 //
+//   * NVFP4 activation quantization ([FP4] §6, step 1 of the native path):
+//     per 16-element block, scale = E4M3(fp32(amax / 6)), codes =
+//     E2M1(fp32(a / scale)) (RNE, ties to even, saturating, sign kept), no
+//     activation global scale (the page names none).
 //   * W8A8 activation quantization ([FP8] §6, "Optional W8A8 Activation
 //     Path": A_deq = fp8_e4m3(A / a_scale) * a_scale): A / a_scale as one
 //     float32 division (IEEE, correctly rounded), E4M3FN by round-to-nearest-
@@ -267,6 +271,53 @@ uint8_t e4m3_rne_satfinite(float f) {
   return (uint8_t)(sign | c);
 }
 
+// E2M1 code of a float32 value: round to nearest, ties to the even mantissa
+// (code parity = mantissa parity), saturating to the largest magnitude 6.
+// The sign of the input is kept, so -0.0 and negative values that round to
+// zero give code 0x8 (negative zero).  Plain search over the 8 magnitudes
+// (codes 0..7 ascend in value).  Finite inputs only.
+uint8_t e2m1_rne_satfinite(float f) {
+  const uint8_t sign = std::signbit(f) ? 0x8 : 0x0;
+  const double a = std::fabs((double)f);
+  if (a >= kE2M1[7]) return (uint8_t)(sign | 7);
+  int lo = 0;
+  while (lo + 1 <= 7 && kE2M1[lo + 1] <= a) ++lo;  // kE2M1[lo] <= a < kE2M1[lo + 1]
+  if (kE2M1[lo] == a) return (uint8_t)(sign | lo);
+  const double dlo = a - kE2M1[lo], dhi = kE2M1[lo + 1] - a;
+  int c;
+  if (dlo < dhi) c = lo;
+  else if (dhi < dlo) c = lo + 1;
+  else c = (lo % 2 == 0) ? lo : lo + 1;
+  return (uint8_t)(sign | c);
+}
+
+// NVFP4 activation quantization, one 16-element block of one row ([FP4] §6,
+// "Native SM120 FP4 x FP4 Path", step 1: "quantize activation A to packed
+// NVFP4 E2M1 with per-16-block E4M3 scales").  The page gives no formula;
+// the reading taken (plainest, no activation global scale since the page
+// names none):
+//   amax  = max |a| over the block (a exact in float32)
+//   scale = E4M3(fp32(amax / 6))              RNE, saturating at 448
+//   q_i   = E2M1(fp32(a_i / e4m3(scale)))     RNE, saturating at 6, sign kept;
+//           a scale that decodes to 0 gives q_i = +-0 (sign of a_i).
+// Writes n codes (n <= 16) and returns the scale byte.
+uint8_t nvfp4_quantize_block(const uint16_t* a, int n, int dtype, uint8_t* codes) {
+  build_e4m3_table();
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    const float v = (float)std::fabs(act_to_double(a[i], dtype));  // exact
+    if (v > amax) amax = v;
+  }
+  const uint8_t sc = e4m3_rne_satfinite(amax / 6.0f);  // one float32 division
+  const float sd = (float)g_e4m3[sc];
+  for (int i = 0; i < n; ++i) {
+    const float x = (float)act_to_double(a[i], dtype);
+    if (sd == 0.0f) codes[i] = std::signbit(x) ? 0x8 : 0x0;
+    else codes[i] = e2m1_rne_satfinite(x / sd);          // one float32 division
+  }
+  return sc;
+}
+
 // One activation element of the W8A8 path: RNE_act(fp32(e4m3(fp32(a / s)) * s)).
 uint16_t fp8_qdq_one(uint16_t a_bits, float a_scale, int dtype) {
   const float a = (float)act_to_double(a_bits, dtype);     // exact
@@ -303,6 +354,51 @@ void orc_fp8_qdq_activation(const uint16_t* A, float a_scale, uint16_t* out, int
                             int dtype) {
   build_e4m3_table();
   for (int64_t i = 0; i < n; ++i) out[i] = fp8_qdq_one(A[i], a_scale, dtype);
+}
+
+int orc_e2m1_from_f32(float f) { return e2m1_rne_satfinite(f); }
+
+// NVFP4 activation quantization of A [M, K] (K even): codes packed two per
+// byte, the even k in the low nibble (the weight layout of [FP4] §2), into
+// codes [M, K / 2]; E4M3 block scales into scales [M, ceil(K / 16)].  A
+// partial last block (K % 16 != 0) takes its amax over the elements it has.
+void orc_nvfp4_quantize_act(const uint16_t* A, int64_t M, int64_t K, int dtype, uint8_t* codes,
+                            uint8_t* scales) {
+  const int64_t S = (K + 15) / 16;
+  for (int64_t m = 0; m < M; ++m) {
+    std::memset(codes + m * (K / 2), 0, (size_t)(K / 2));
+    for (int64_t b = 0; b < S; ++b) {
+      const int n = (int)std::min<int64_t>(16, K - 16 * b);
+      uint8_t q[16];
+      scales[m * S + b] = nvfp4_quantize_block(A + m * K + 16 * b, n, dtype, q);
+      for (int i = 0; i < n; ++i) {
+        const int64_t k = 16 * b + i;
+        uint8_t& byte = codes[m * (K / 2) + k / 2];
+        byte = (uint8_t)(byte | ((k % 2 == 0) ? q[i] : (q[i] << 4)));
+      }
+    }
+  }
+}
+
+// NVFP4 activation quantize-dequantize: out = RNE_act(e2m1(q) * e4m3(scale))
+// per element.  The product has at most 6 significant bits and lies in
+// [2^-10, 2688] (or is zero), so it is exact in float32 and in both
+// activation types: the rounding to the activation type is exact.
+void orc_nvfp4_qdq_act(const uint16_t* A, int64_t M, int64_t K, int dtype, uint16_t* out) {
+  build_e4m3_table();
+  const int64_t S = (K + 15) / 16;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t b = 0; b < S; ++b) {
+      const int n = (int)std::min<int64_t>(16, K - 16 * b);
+      uint8_t q[16];
+      const uint8_t sc = nvfp4_quantize_block(A + m * K + 16 * b, n, dtype, q);
+      const float sd = (float)g_e4m3[sc];
+      for (int i = 0; i < n; ++i) {
+        const float v = (float)kE2M1[q[i]] * sd;  // exact
+        out[m * K + 16 * b + i] = rne_to_act(f32_bits(v), dtype);
+      }
+    }
+  }
 }
 
 // Standalone FP4 dequantize (bit-exact contract):

@@ -427,3 +427,127 @@ def test_fp8_qdq_activation_hand_cases():
         out = oracle.fp8_qdq_activation(A, 2.0, dtype)
         got = [oracle.act_to_double(int(b), dtype) for b in out]
         assert got == [6.5, 7.0, -7.0, 896.0, 0.0], (dtype, got)
+
+
+# --- NVFP4 activation quantization (FP4 page §6, step 1 of the native path) ---
+
+def _nvfp4_golden_cases():
+    cases, cur = {}, None
+    for ln in _golden_lines("nvfp4_activation.txt"):
+        if ln[0] == "case":
+            cur = cases.setdefault(ln[1], {})
+        elif ln[0] in ("x", "qdq"):
+            cur[ln[0]] = [float(v) for v in ln[1:]]
+        elif ln[0] == "scale":
+            cur["scale"] = int(ln[1], 16)
+        elif ln[0] == "packed":
+            cur["packed"] = [int(v, 16) for v in ln[1:]]
+    return cases
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+def test_nvfp4_activation_golden_blocks(dtype):
+    for name, c in _nvfp4_golden_cases().items():
+        A = wl.act_bits(np.array([c["x"]]), dtype)
+        codes, scales = oracle.nvfp4_quantize_activation(A, dtype)
+        assert scales.tolist() == [[c["scale"]]], name
+        assert codes.tolist() == [c["packed"]], name
+        q = oracle.nvfp4_qdq_activation(A, dtype)
+        got = [oracle.act_to_double(int(b), dtype) for b in q[0]]
+        assert got == c["qdq"], name
+        # signs of zeros as listed
+        assert [math.copysign(1, g) for g in got] == [math.copysign(1, v) for v in c["qdq"]], name
+
+
+def test_e2m1_encode_roundtrip_every_code():
+    """Every E2M1 value encodes back to its own code (-0.0 keeps its sign)."""
+    table = _e2m1_golden()
+    for c in range(16):
+        assert oracle.e2m1_from_f32(np.float32(table[c])) == c or (c == 0 and table[c] == 0.0)
+    assert oracle.e2m1_from_f32(np.float32(-0.0)) == 0x8
+
+
+def test_e2m1_encode_ties_nearest_and_saturation():
+    """Midpoints of neighbouring magnitudes go to the even code; a hair off
+    goes to the nearer one; beyond 6 saturates; signs mirror."""
+    table = _e2m1_golden()
+    for c in range(7):
+        lo, hi = table[c], table[c + 1]
+        mid = np.float32((lo + hi) / 2)
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e2m1_from_f32(mid) == even, c
+        assert oracle.e2m1_from_f32(-mid) == 0x8 | even, c
+        assert oracle.e2m1_from_f32(np.nextafter(mid, np.float32(-1))) == c, c
+        assert oracle.e2m1_from_f32(np.nextafter(mid, np.float32(10))) == c + 1, c
+    for v in (6.0, 6.5, 7.0, 100.0, 1e30):
+        assert oracle.e2m1_from_f32(v) == 7
+        assert oracle.e2m1_from_f32(-v) == 15
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+def test_nvfp4_activation_exact_grid_round_trip(dtype):
+    """Blocks built from E2M1 values times 2^e with a +-6 entry (so amax/6 is
+    exactly 2^e, an E4M3 value) quantize to exactly those codes and scales:
+    pins the amax/6 rule, the division, the sign and the nibble order."""
+    r = np.random.Generator(np.random.PCG64(31))
+    table = np.array([_e2m1_golden()[c] for c in range(16)])
+    M, K = 6, 64
+    for e in (-6, -2, 0, 3, 6):
+        codes = r.integers(0, 16, (M, K))
+        codes[:, ::16] = r.choice([7, 15], (M, K // 16))  # every block reaches |6|
+        x = table[codes] * 2.0 ** e
+        A = wl.act_bits(x, dtype)
+        pc, sc = oracle.nvfp4_quantize_activation(A, dtype)
+        want_scale = oracle.e4m3_from_f32(2.0 ** e)
+        assert (sc == want_scale).all(), e
+        assert oracle.e4m3_value(want_scale) == 2.0 ** e
+        assert np.array_equal(pc & 0xF, codes[:, 0::2]), e
+        assert np.array_equal(pc >> 4, codes[:, 1::2]), e
+        q = oracle.nvfp4_qdq_activation(A, dtype)
+        assert np.array_equal(q, A), e  # the grid values come back unchanged
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+def test_nvfp4_activation_error_bound_and_consistency(dtype):
+    """Random activations (three magnitudes, the smallest one reaching
+    subnormal E4M3 scales): an element within 6 scales is off by at most
+    half the local E2M1 gap times the scale (gaps 0.5 below 2, 1 up to 4, 2
+    up to 6); one beyond is exactly +-6 scales; with a normal E4M3 scale no
+    element is beyond 6 * (1 + 2^-4) scales (amax / 6 rounds within 2^-4).
+    qdq equals e2m1(code) * e4m3(scale) read back from the packed codes."""
+    r = np.random.Generator(np.random.PCG64(5))
+    M, K = 8, 400  # 25 blocks per row
+    table = np.array([_e2m1_golden()[c] for c in range(16)])
+    for sigma in (1.0, 30.0, 1e-2):
+        A = wl.act_bits(r.normal(0, sigma, (M, K)), dtype)
+        x = np.array([[oracle.act_to_double(int(b), dtype) for b in row] for row in A])
+        pc, sc = oracle.nvfp4_quantize_activation(A, dtype)
+        q = oracle.nvfp4_qdq_activation(A, dtype)
+        qv = np.array([[oracle.act_to_double(int(b), dtype) for b in row] for row in q])
+        sd = np.repeat(np.array([[oracle.e4m3_value(int(b)) for b in row] for row in sc]), 16,
+                       axis=1)[:, :K]
+        normal = np.repeat((sc & 0x78) != 0, 16, axis=1)[:, :K]
+        u = np.abs(x) / sd
+        inside = u <= 6.0
+        half_gap = np.where(u < 2, 0.25, np.where(u < 4, 0.5, 1.0))
+        assert np.all(np.abs(qv - x)[inside] <= (half_gap * sd)[inside]), sigma
+        assert np.array_equal(qv[~inside], (np.sign(x) * 6 * sd)[~inside]), sigma
+        assert np.all(u[normal] <= 6 * (1 + 2.0 ** -4)), sigma
+        codes = np.empty((M, K), dtype=np.int64)
+        codes[:, 0::2] = pc & 0xF
+        codes[:, 1::2] = pc >> 4
+        assert np.array_equal(qv, table[codes] * sd), sigma
+
+
+def test_nvfp4_activation_partial_last_block():
+    """K = 40: the last block has 8 elements and takes its amax over those
+    only (a large value in the first block does not reach it)."""
+    x = np.zeros((1, 40))
+    x[0, :16] = 100.0
+    x[0, 32:40] = [6.0, 3.0, -1.5, 0.5, 0.0, 2.0, -4.0, 1.0]  # amax 6 -> scale 1.0
+    A = wl.act_bits(x, oracle.BF16)
+    pc, sc = oracle.nvfp4_quantize_activation(A, oracle.BF16)
+    assert sc.shape == (1, 3)
+    assert sc[0, 2] == 0x38 and sc[0, 1] == 0x00
+    # codes 7 5 11 1 0 4 14 2 -> bytes (even k low) 0x57 0x1B 0x40 0x2E
+    assert pc[0, 16:20].tolist() == [0x57, 0x1B, 0x40, 0x2E]

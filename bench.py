@@ -325,6 +325,33 @@ def bench_headline(gpu, args, rank, world, barrier_sync):
                 h2d=M * K * 2, d2h=M * N * 2)
 
 
+def actq_bytes(M, K):
+    """NVFP4 activation quantization: read A, write codes and scales."""
+    return 2 * M * K + M * K // 2 + M * ((K + 15) // 16)
+
+
+def bench_actq(gpu, args, hbm):
+    """NVFP4 activation quantization of the 8K-token prefill activation
+    (M = 8192, K = 5120, BF16): a graph of launches over two distinct inputs
+    and outputs (215 MB, above L2), per launch."""
+    torch = gpu.torch
+    wq = gpu.wq
+    M, K = 8192, 5120
+    As = [torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16) for _ in range(2)]
+    outs = [(torch.empty(M, K // 2, dtype=torch.uint8, device=gpu.dev),
+             torch.empty(M, K // 16, dtype=torch.uint8, device=gpu.dev)) for _ in range(2)]
+
+    def step():
+        for A, (pc, sc) in zip(As, outs):
+            wq.fp4_quantize_activation(A, out_packed=pc, out_scale=sc, stream=gpu.stream)
+    g = gpu.graph(step)
+    reps = max(5, args.steps // 5)
+    dt = gpu.time_graph(g, reps, 2) / (reps * 2)
+    gbs = actq_bytes(M, K) / dt / 1e9
+    return {f"nvfp4_act_quantize_M{M}_K{K}": {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                                                "us": round(dt * 1e6, 2)}}
+
+
 def bench_also(gpu, args, peaks):
     torch = gpu.torch
     wq = gpu.wq
@@ -434,6 +461,7 @@ def bench_also(gpu, args, peaks):
                                            "us": round(dt * 1e6, 2)}
             del g
         del lys
+    out.update(bench_actq(gpu, args, hbm))
     # Whole decode step: one CUDA graph of 120 weight-only GEMVs shaped like a
     # 27B-class decoder (hidden 5120, MLP 17408): per layer four 5120 x 5120
     # projections, gate and up 17408 x 5120, down 5120 x 17408 (17 layers), then

@@ -18,6 +18,9 @@ Torch-tensor wrappers (same names):
 * ``fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias=None, block_size=128, out=None)``
   and ``fp8_quantize_dequantize_activation(A, a_scale)`` ("MatMulBlockQuantizedFp8Weight -
   CUDA Operator Documentation" §6, the optional W8A8 activation path).
+* ``fp4_quantize_activation(A)`` and ``fp4_quantize_dequantize_activation(A)``
+  ("MatMulBlockQuantizedFp4Weight - CUDA Operator Documentation" §6, step 1 of the
+  native FP4 x FP4 path: packed E2M1 codes with per-16 E4M3 scales).
 * ``fp4_dequantize(B_packed, weight_scale, weight_scale_2, block_size=16,
   dtype=torch.bfloat16, out=None)`` and ``fp8_dequantize(...)``.
 """
@@ -31,6 +34,7 @@ import threading
 __all__ = [
     "WqmmError", "lib", "library_path", "fp4_weight_matmul", "fp8_weight_matmul",
     "fp8_weight_matmul_w8a8", "fp8_quantize_dequantize_activation",
+    "fp4_quantize_activation", "fp4_quantize_dequantize_activation",
     "fp4_dequantize", "fp8_dequantize", "device_status", "FP16", "BF16",
 ]
 
@@ -49,7 +53,8 @@ STATUS = {
 
 # Exported C symbols, in header order.
 SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
-           "fp8_quantize_dequantize_activation", "fp4_dequantize", "fp8_dequantize",
+           "fp8_quantize_dequantize_activation", "fp4_quantize_activation",
+           "fp4_quantize_dequantize_activation", "fp4_dequantize", "fp8_dequantize",
            "wqmm_status_string", "wqmm_device_status", "wqmm_version")
 
 
@@ -80,6 +85,8 @@ def lib():
         L.fp8_weight_matmul.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
         L.fp8_weight_matmul_w8a8.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P]
         L.fp8_quantize_dequantize_activation.argtypes = [P, P, P, I64, I, P]
+        L.fp4_quantize_activation.argtypes = [P, P, P, I64, I64, I, P]
+        L.fp4_quantize_dequantize_activation.argtypes = [P, P, I64, I64, I, P]
         L.fp4_dequantize.argtypes = [P, P, P, P, I64, I64, I, I, P]
         L.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, I, P]
         L.wqmm_status_string.argtypes = [I]
@@ -204,6 +211,42 @@ def fp8_quantize_dequantize_activation(A, a_scale, out=None, stream=None):
     st = lib().fp8_quantize_dequantize_activation(_ptr(A), _ptr(a_scale), _ptr(out), A.numel(),
                                                   _dt(A.dtype), _stream(stream))
     _check(st, "fp8_quantize_dequantize_activation")
+    return out
+
+
+def _rows_k(A):
+    K = A.shape[-1]
+    return A.numel() // K if K else 0, K
+
+
+def fp4_quantize_activation(A, out_packed=None, out_scale=None, stream=None):
+    """NVFP4 quantization of an activation (FP4 page §6, step 1): returns
+    (A_packed [..., K/2] uint8, A_scale [..., ceil(K/16)] uint8 E4M3)."""
+    torch = _torch()
+    _need_cuda(A, out_packed, out_scale)
+    M, K = _rows_k(A)
+    lead = tuple(A.shape[:-1])
+    if out_packed is None:
+        out_packed = torch.empty(lead + (K // 2,), dtype=torch.uint8, device=A.device)
+    if out_scale is None:
+        out_scale = torch.empty(lead + ((K + 15) // 16,), dtype=torch.uint8, device=A.device)
+    st = lib().fp4_quantize_activation(_ptr(A), _ptr(out_packed), _ptr(out_scale), M, K,
+                                       _dt(A.dtype), _stream(stream))
+    _check(st, "fp4_quantize_activation")
+    return out_packed, out_scale
+
+
+def fp4_quantize_dequantize_activation(A, out=None, stream=None):
+    """e2m1(code) * e4m3(scale) of fp4_quantize_activation, in A's dtype
+    (exact); feeding it to fp4_weight_matmul gives the FP4 x FP4 numerics."""
+    torch = _torch()
+    _need_cuda(A, out)
+    M, K = _rows_k(A)
+    if out is None:
+        out = torch.empty_like(A)
+    st = lib().fp4_quantize_dequantize_activation(_ptr(A), _ptr(out), M, K, _dt(A.dtype),
+                                                  _stream(stream))
+    _check(st, "fp4_quantize_dequantize_activation")
     return out
 
 

@@ -259,6 +259,31 @@ int fp8_quantize_dequantize_activation(const void* A, const float* a_scale, void
                                    static_cast<cudaStream_t>(stream));
 }
 
+int fp4_quantize_activation(const void* A, uint8_t* A_packed, uint8_t* A_scale, int64_t M,
+                            int64_t K, int dtype, void* stream) {
+  if (dtype != WQMM_FP16 && dtype != WQMM_BF16) return WQMM_ERR_INVALID_ARG;
+  if (M < 0 || K < 0 || K % 2 != 0) return WQMM_ERR_INVALID_ARG;
+  if (M >= kMaxDim || K >= kMaxDim) return WQMM_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return WQMM_OK;
+  if (!A || !A_packed || !A_scale) return WQMM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(A_packed) || !aligned16(A_scale)) return WQMM_ERR_MISALIGNED;
+  if (current_device() < 0) return WQMM_ERR_CUDA;
+  return launch_nvfp4_quantize_activation(A, A_packed, A_scale, M, K, dtype,
+                                          static_cast<cudaStream_t>(stream));
+}
+
+int fp4_quantize_dequantize_activation(const void* A, void* out, int64_t M, int64_t K, int dtype,
+                                       void* stream) {
+  if (dtype != WQMM_FP16 && dtype != WQMM_BF16) return WQMM_ERR_INVALID_ARG;
+  if (M < 0 || K < 0 || K % 2 != 0) return WQMM_ERR_INVALID_ARG;
+  if (M >= kMaxDim || K >= kMaxDim) return WQMM_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return WQMM_OK;
+  if (!A || !out) return WQMM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(out)) return WQMM_ERR_MISALIGNED;
+  if (current_device() < 0) return WQMM_ERR_CUDA;
+  return launch_nvfp4_qdq_activation(A, out, M, K, dtype, static_cast<cudaStream_t>(stream));
+}
+
 int fp4_dequantize(const uint8_t* B_packed, const uint8_t* weight_scale,
                    const float* weight_scale_2, void* out, int64_t N, int64_t K, int block_size,
                    int dtype, void* stream) {

@@ -75,6 +75,14 @@ bool gemv_tma_supports(const GemvArgs& a);
 int launch_fp8_qdq_activation(const void* A, const float* a_scale, void* out, int64_t n,
                               int dtype, cudaStream_t st);
 
+// ---- NVFP4 activation quantization (wqmm_actq.cu) ----
+// codes [M, K/2] (two per byte, even k low), scales [M, ceil(K/16)] E4M3.
+int launch_nvfp4_quantize_activation(const void* A, uint8_t* codes, uint8_t* scales, int64_t M,
+                                     int64_t K, int dtype, cudaStream_t st);
+// out [M, K] = e2m1(code) * e4m3(scale) in the activation type (exact).
+int launch_nvfp4_qdq_activation(const void* A, void* out, int64_t M, int64_t K, int dtype,
+                                cudaStream_t st);
+
 // ---- fused tcgen05 GEMM for large M (wqmm_gemm.cu) ----
 // Returns kUnsupported if the shape cannot take this path.
 int launch_gemm(const GemvArgs& a, cudaStream_t st);

@@ -138,6 +138,40 @@ int fp8_quantize_dequantize_activation(const void* A, const float* a_scale, void
                                        int64_t count, int dtype, void* stream);
 
 /*
+ * fp4_quantize_activation -- NVFP4 quantization of an activation, the first
+ * step of the native FP4 x FP4 path of [FP4] §6 ("quantize activation A to
+ * packed NVFP4 E2M1 with per-16-block E4M3 scales").  The page gives no
+ * formula; per 16-element block of each row of A:
+ *     scale = E4M3(fp32(amax / 6))          RNE, saturating at 448
+ *     code  = E2M1(fp32(a / e4m3(scale)))   RNE, ties to the even code,
+ *                                           saturating at 6, sign of a kept;
+ *                                           a zero scale gives +-0
+ * (no activation global scale: the page names none).  Bit-exact contract.
+ *   A         [M, K] dtype, row-major (16-byte aligned); finite values.
+ *   A_packed  [M, K/2] uint8: two codes per byte, the even k in the low
+ *             nibble (the weight layout of [FP4] §2).
+ *   A_scale   [M, ceil(K/16)] uint8 E4M3FN; a partial last block (K % 16 != 0)
+ *             takes its amax over the elements it has.
+ * Errors: K odd, M or K < 0, or a NULL pointer with M*K > 0 -> INVALID_ARG;
+ * a base pointer not 16-byte aligned -> MISALIGNED; M*K == 0 -> OK, no launch.
+ */
+int fp4_quantize_activation(const void* A, uint8_t* A_packed, uint8_t* A_scale, int64_t M,
+                            int64_t K, int dtype, void* stream);
+
+/*
+ * fp4_quantize_dequantize_activation -- out = e2m1(code) * e4m3(scale) of
+ * fp4_quantize_activation, element by element in dtype ([M, K], 16-byte
+ * aligned).  The value has at most 6 significant bits in [2^-10, 2688] (or
+ * is zero), so it is exact in FP16 and BF16, and
+ *     fp4_weight_matmul(fp4_quantize_dequantize_activation(A), B, ...)
+ * computes the activation-and-weight FP4 product of [FP4] §6 (exact
+ * products, FP32 accumulation) with the weight-only kernels.  Errors as for
+ * fp4_quantize_activation.
+ */
+int fp4_quantize_dequantize_activation(const void* A, void* out, int64_t M, int64_t K, int dtype,
+                                       void* stream);
+
+/*
  * fp4_dequantize -- expand an NVFP4 weight to the activation type.
  * [FP4] §2 formula, §5 step 1; [BLOG] vectorised dequant.
  *   out[n, k] = RNE_dtype( fp32( fp32(e2m1 * e4m3) * weight_scale_2 ) )

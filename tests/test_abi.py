@@ -101,6 +101,24 @@ def test_dequant_argument_checks(L):
     assert L.fp8_dequantize(FAKE_ODD, FAKE, FAKE, 4, 32, 16, 1, None) == 3
 
 
+def test_activation_quantize_argument_checks(L):
+    """NVFP4 activation quantization: host-side checks only (no launch)."""
+    q, qdq = L.fp4_quantize_activation, L.fp4_quantize_dequantize_activation
+    assert q(FAKE, FAKE, FAKE, 4, 33, 1, None) == 1           # odd K
+    assert q(FAKE, FAKE, FAKE, -1, 32, 1, None) == 1          # negative M
+    assert q(FAKE, FAKE, FAKE, 4, 32, 2, None) == 1           # dtype
+    assert q(FAKE, None, FAKE, 4, 32, 1, None) == 1           # NULL output
+    assert q(FAKE_ODD, FAKE, FAKE, 4, 32, 1, None) == 3       # misaligned A
+    assert q(FAKE, FAKE, FAKE_ODD, 4, 32, 0, None) == 3       # misaligned scales
+    assert q(None, None, None, 0, 32, 1, None) == 0           # empty
+    assert q(None, None, None, 5, 0, 1, None) == 0
+    assert q(FAKE, FAKE, FAKE, 1 << 31, 32, 1, None) == 2     # too large
+    assert qdq(FAKE, FAKE, 4, 31, 1, None) == 1
+    assert qdq(FAKE, None, 4, 32, 1, None) == 1
+    assert qdq(FAKE, FAKE_ODD, 4, 32, 1, None) == 3
+    assert qdq(None, None, 0, 32, 0, None) == 0
+
+
 def test_torch_wrappers_refuse_cpu_tensors(L):
     import torch
     A = torch.zeros(1, 32, dtype=torch.bfloat16)

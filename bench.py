@@ -624,6 +624,13 @@ def run_only(name, m, reps):
         W = torch.empty(N, K, dtype=torch.bfloat16, device=gpu.dev)
         fn = lambda: wq.fp4_dequantize(ly["B"], ly["ws"], ly["ws2"], 16, out=W, stream=gpu.stream)
         work = dequant_bytes(N, K) / 1e9, "GB/s"
+    elif name == "actq":
+        M, K = (m or 8192), 5120
+        A = torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16)
+        pc = torch.empty(M, K // 2, dtype=torch.uint8, device=gpu.dev)
+        sc = torch.empty(M, K // 16, dtype=torch.uint8, device=gpu.dev)
+        fn = lambda: wq.fp4_quantize_activation(A, out_packed=pc, out_scale=sc, stream=gpu.stream)
+        work = actq_bytes(M, K) / 1e9, "GB/s"
     elif name == "fp8_gemv":
         M, N, K = (m or 4), 5120, 5120
         B = gpu.t(wl.gen_fp8_weight(N, K, 300))
@@ -652,7 +659,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--only", default=None,
                     help="run one workload (gemv, lm_head, prefill_gate_up, prefill_down, "
-                         "dequant, fp8_gemv, decode_step) a few times, for profilers")
+                         "dequant, actq, fp8_gemv, decode_step) a few times, for profilers")
     ap.add_argument("--m", type=int, default=None, help="rows of A for --only")
     ap.add_argument("--reps", type=int, default=3, help="timed launches for --only")
     args = ap.parse_args()

@@ -15,12 +15,13 @@
 // type: at most 6 significant bits in [2^-10, 2688] (or zero), exact, so a
 // weight-only matmul of it has the numerics of the FP4 x FP4 product.
 //
-// One thread per block: two 16-byte loads, two float32 divisions per block
-// (the scale and its reciprocal), a multiply and two adds per element (an
-// exact stand-in for the division, see below), the E2M1 and E4M3
-// conversions in hardware, one
-// 8-byte code store and one scale byte (or two 16-byte stores for the
-// quantize-dequantize form).  HBM-bound: 2 bytes read per element.
+// One thread per block: two 16-byte loads, amax on packed 16-bit pairs, two
+// float32 divisions per block (the scale and its reciprocal), a fused
+// multiply-add and an add per element (an exact stand-in for the division,
+// see below), the E2M1 and E4M3 conversions in hardware, the sign bits
+// gathered with byte permutes, one 8-byte code store and one scale byte (or
+// two 16-byte stores for the quantize-dequantize form).  Bound by HBM
+// (2 bytes read per element) and, before that, by the ALU work per element.
 #include "wqmm_device.cuh"
 
 namespace wqmm {
@@ -38,17 +39,50 @@ __device__ __forceinline__ uint32_t e4m3_of(float s) {
   return r & 0xFFu;
 }
 
-// E2M1 code pair (low nibble = lo) from two non-negative magnitudes (RNE,
-// saturating, in hardware) and the signs of two values (xlo, xhi): -0.0 and
-// negatives that round to zero give code 0x8.
-__device__ __forceinline__ uint32_t e2m1_pair(float xlo, float xhi, float mlo, float mhi) {
+// Eight E2M1 magnitude codes (RNE, saturating, in hardware) from eight
+// non-negative float32 values, packed four bytes to a word: byte j holds
+// elements 2j (low nibble) and 2j + 1.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&m)[8]) {
   uint32_t r;
-  asm("{ .reg .b8 c; .reg .b32 w; cvt.rn.satfinite.e2m1x2.f32 c, %2, %1;\n\t"
-      "mov.b32 w, {c, c, c, c}; and.b32 %0, w, 0xFF; }"
+  asm("{ .reg .b8 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3}; }"
       : "=r"(r)
-      : "f"(mlo), "f"(mhi));
-  r |= (__float_as_uint(xlo) >> 31) << 3;
-  r |= (__float_as_uint(xhi) >> 31) << 7;
+      : "f"(m[0]), "f"(m[1]), "f"(m[2]), "f"(m[3]), "f"(m[4]), "f"(m[5]), "f"(m[6]), "f"(m[7]));
+  return r;
+}
+
+// Sign bits of the eight activation values in words w0..w3 (two 16-bit
+// values per word, the even element low) placed where e2m1x8 puts the codes:
+// bit 3 of byte j for element 2j, bit 7 for element 2j + 1.  So -0.0 and
+// negatives that round to zero give code 0x8.
+__device__ __forceinline__ uint32_t e2m1x8_signs(uint32_t w0, uint32_t w1, uint32_t w2,
+                                                 uint32_t w3) {
+  const uint32_t t = __byte_perm(w0, w1, 0x7531);   // high bytes: elements 0..3
+  const uint32_t u = __byte_perm(w2, w3, 0x7531);   // elements 4..7
+  const uint32_t ev = __byte_perm(t, u, 0x6420);    // elements 0, 2, 4, 6
+  const uint32_t od = __byte_perm(t, u, 0x7531);    // elements 1, 3, 5, 7
+  return ((ev >> 4) & 0x08080808u) | (od & 0x80808080u);
+}
+
+// Largest of the two 16-bit halves of non-negative activation words (their
+// float order is their unsigned order), as a float32.
+template <int DT>
+__device__ __forceinline__ float act_pair_max(uint32_t v) {
+  const float lo = act_bits_to_f32<DT>(v & 0xFFFFu), hi = act_bits_to_f32<DT>(v >> 16);
+  return fmaxf(lo, hi);
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t max2_act(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if constexpr (DT == 1)
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  else
+    asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
@@ -77,55 +111,56 @@ __global__ void __launch_bounds__(kAqThreads)
       w[i] = lo | (hi << 16);
     }
   }
-  float x[16];
-  float amax = 0.0f;
+  // amax on the packed magnitudes: sign bits cleared, pairwise max.
+  uint32_t aw[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = act_bits_to_f32<DT>(w[i] & 0xFFFFu);
-    x[2 * i + 1] = act_bits_to_f32<DT>(w[i] >> 16);
-    amax = fmaxf(amax, fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1])));
-  }
+  for (int i = 0; i < 8; ++i) aw[i] = w[i] & 0x7FFF7FFFu;
+  const uint32_t m01 = max2_act<DT>(aw[0], aw[1]), m23 = max2_act<DT>(aw[2], aw[3]);
+  const uint32_t m45 = max2_act<DT>(aw[4], aw[5]), m67 = max2_act<DT>(aw[6], aw[7]);
+  const float amax =
+      act_pair_max<DT>(max2_act<DT>(max2_act<DT>(m01, m23), max2_act<DT>(m45, m67)));
   const uint32_t sc = e4m3_of(__fdiv_rn(amax, 6.0f));
   const float sd = e4m3_to_f32(sc);
-  // The E2M1 code of fp32(a / sd) without a division per element: p = a *
-  // RN(1 / sd) is within 2^-23 (relative) of a / sd, and a quotient that is
+  // The E2M1 code of fp32(a / sd) without a division per element: |a| *
+  // RN(1 / sd) is within 2^-24 (relative) of |a| / sd, and a quotient that is
   // not one of the E2M1 rounding midpoints (0.25, 0.75, ..., 5) lies at least
   // 2^-11 (relative) away from all of them (a has at most 11 significant
-  // bits, sd 4).  Snapping p to a grid of 2^-15 ((p + 384) - 384, valid
-  // below 8; larger values saturate either way) moves every exact midpoint
-  // onto the midpoint and keeps every other value on its side, so the
-  // hardware round-to-nearest-even conversion gives the code of the division.
+  // bits, sd 4).  Snapping the product to a grid of 2^-15 with one fused
+  // multiply-add (RN(|a| * inv + 384) - 384, exact subtraction; valid below
+  // 8, larger values saturate either way) moves every exact midpoint onto
+  // the midpoint and keeps every other value on its side, so the hardware
+  // round-to-nearest-even conversion gives the code of the division.
   // A zero scale gives inv = 0 and codes +-0.
   const float inv = sd == 0.0f ? 0.0f : __fdiv_rn(1.0f, sd);
-  auto snap = [&](float v) {
-    return __fadd_rn(__fadd_rn(fabsf(v) * inv, 384.0f), -384.0f);
-  };
-  uint32_t q[8];  // one code pair (byte) per word
+  float mag[2][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = e2m1_pair(x[2 * i], x[2 * i + 1], snap(x[2 * i]),
-                                              snap(x[2 * i + 1]));
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float v = act_bits_to_f32<DT>(h ? (aw[i] >> 16) : (aw[i] & 0xFFFFu));
+      mag[i >> 2][2 * (i & 3) + h] = __fadd_rn(__fmaf_rn(v, inv, 384.0f), -384.0f);
+    }
+  }
+  const uint32_t lo4 = e2m1x8(mag[0]) | e2m1x8_signs(w[0], w[1], w[2], w[3]);
+  const uint32_t hi4 = e2m1x8(mag[1]) | e2m1x8_signs(w[4], w[5], w[6], w[7]);
   if constexpr (!QDQ) {
     uint8_t* c = codes + m * (K / 2) + k0 / 2;
-    const uint32_t lo4 = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-    const uint32_t hi4 = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
     if (n == 16 && (reinterpret_cast<uintptr_t>(c) & 7u) == 0) {
       *reinterpret_cast<uint2*>(c) = make_uint2(lo4, hi4);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (2 * i < n) c[i] = (uint8_t)q[i];
+        if (2 * i < n) c[i] = (uint8_t)((i < 4 ? lo4 : hi4) >> (8 * (i & 3)));
     }
     scales[blk] = (uint8_t)sc;
   } else {
     uint32_t o[8];
+    uint32_t h[8];
+    e2m1x8_to_f16x8(lo4, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
+    e2m1x8_to_f16x8(hi4, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      uint32_t h;
-      asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1;\n\t"
-          "cvt.rn.f16x2.e2m1x2 %0, b0; }"
-          : "=r"(h)
-          : "r"(q[i]));
-      const float2 e = f16x2_to_f32x2(h);
+      const float2 e = f16x2_to_f32x2(h[i]);
       o[i] = pack2_rn<DT>(e.x * sd, e.y * sd);  // exact products
     }
     uint16_t* y = out + m * K + k0;

@@ -257,26 +257,35 @@ class Gpu:
         return statistics.median(ts)
 
 
-def gemv_chain(gpu, M, N, K, L, kind="fp4"):
-    """L chained layers: layer i reads the previous layer's output."""
+def gemv_chain(gpu, M, N, K, L, kind="fp4", act="bf16", ws2=0.0125, feed=True):
+    """L chained layers: layer i reads the previous layer's output (feed=True)
+    or every layer reads the step's input (feed=False: for FP8 weights, which
+    scale the activation by ~80 per layer and would leave the BF16 range; the
+    launches are stream-ordered either way, each layer waiting for the
+    previous one to complete, so the timing is the same)."""
     torch = gpu.torch
     wq = gpu.wq
+    tdt = torch.bfloat16 if act == "bf16" else torch.float16
     if kind == "fp4":
-        layers = gpu.fp4_layers(M, N, K, L)
+        layers = gpu.fp4_layers(M, N, K, L, ws2=ws2)
     else:
         layers = []
         for i in range(L):
             layers.append(dict(B=gpu.t(wl.gen_fp8_weight(N, K, 300 + i)),
                                s=gpu.t(wl.gen_fp8_scale(N, wl.scale_cols(K, 128), 0.001, 0.02,
                                                         300 + i))))
-    bufs = [gpu.t(wl.gen_activation(M, K, 1, 7).view(np.int16), torch.bfloat16),
-            torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)]
-    # N == K, so outputs ping-pong with inputs.
+    # bufs[0] holds the step's input and is never written, so every replay
+    # starts from the same activation; the layers ping-pong between bufs[1]
+    # and bufs[2] (N == K), layer i + 1 reading layer i's output.
+    bufs = [gpu.t(wl.gen_activation(M, K, 1 if act == "bf16" else 0, 7).view(np.int16), tdt),
+            torch.empty(M, N, dtype=tdt, device=gpu.dev),
+            torch.empty(M, N, dtype=tdt, device=gpu.dev)]
     assert N == K
 
     def step():
         for i, ly in enumerate(layers):
-            a, y = bufs[i % 2], bufs[(i + 1) % 2]
+            a = bufs[0] if (i == 0 or not feed) else bufs[1 + (i - 1) % 2]
+            y = bufs[1 + i % 2]
             if kind == "fp4":
                 wq.fp4_weight_matmul(a, ly["B"], ly["ws"], ly["ws2"], None, 16, out=y,
                                      stream=gpu.stream)
@@ -303,7 +312,7 @@ def bench_headline(gpu, args, rank, world, barrier_sync):
         for _ in range(2):
             bufs[0].copy_(h_in, non_blocking=True)
             g.replay()
-            h_out.copy_(bufs[L % 2], non_blocking=True)
+            h_out.copy_(bufs[1 + (L - 1) % 2], non_blocking=True)
         gpu.stream.synchronize()
         if barrier_sync:
             barrier_sync()
@@ -314,7 +323,7 @@ def bench_headline(gpu, args, rank, world, barrier_sync):
         for _ in range(args.steps):
             bufs[0].copy_(h_in, non_blocking=True)
             g.replay()
-            h_out.copy_(bufs[L % 2], non_blocking=True)
+            h_out.copy_(bufs[1 + (L - 1) % 2], non_blocking=True)
         e1.record(gpu.stream)
         e1.synchronize()
         wall = time.perf_counter() - t0
@@ -377,7 +386,28 @@ def bench_also(gpu, args, peaks):
     gbs = gemv_bytes(M, N, K, bias=True) * reps / dt / 1e9
     out["lm_head_M4_N152064_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
                                        "us": round(dt / reps * 1e6, 2)}
-    del g, ly
+    # The same lm_head with FP16 activations and bias (the decode of each
+    # weight pair folds its scale with one f16x2 multiply instead of two
+    # mixed multiplies and a BF16 pack).
+    A16 = gpu.t(wl.gen_activation(M, K, 0, 9).view(np.int16), torch.float16)
+    b16 = gpu.t(wl.gen_bias(N, 0, 0.02, 500).view(np.int16), torch.float16)
+    Y16 = torch.empty(M, N, dtype=torch.float16, device=gpu.dev)
+    g16 = gpu.graph(lambda: wq.fp4_weight_matmul(A16, ly["B"], ly["ws"], ly["ws2"], b16, 16,
+                                                 out=Y16, stream=gpu.stream))
+    dt = gpu.time_graph(g16, reps, 3)
+    gbs = gemv_bytes(M, N, K, bias=True) * reps / dt / 1e9
+    out["lm_head_fp16_M4_N152064_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                                            "us": round(dt / reps * 1e6, 2)}
+    # The M = 4 chain with FP16 activations (weight_scale_2 = 0.002 keeps the
+    # chained values inside the FP16 range; the time does not depend on it).
+    step, _, _ = gemv_chain(gpu, 4, 5120, 5120, LAYERS, act="fp16", ws2=0.002)
+    gc = gpu.graph(step)
+    nrep = max(5, args.steps // 2)
+    dtc = gpu.time_graph(gc, nrep, 2)
+    gbs = gemv_bytes(4, 5120, 5120) * LAYERS * nrep / dtc / 1e9
+    out["gemv_fp16_M4_N5120_K5120"] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                                       "us_per_layer": round(dtc / (nrep * LAYERS) * 1e6, 2)}
+    del g, g16, gc, ly
     # Prefill GEMMs (tensor-bound), L2 flushed before each timed launch.
     tf_peak = peaks["bf16_tflops"]
     for shape, (N, K) in (("gate_up", (17408, 5120)), ("down", (5120, 17408))):
@@ -424,7 +454,7 @@ def bench_also(gpu, args, peaks):
     # FP8 decode GEMV chain (secondary format), M = 1, 4, 8.
     reps = max(5, args.steps // 2)
     for M in (1, 4, 8):
-        step, _, _ = gemv_chain(gpu, M, 5120, 5120, LAYERS, kind="fp8")
+        step, _, _ = gemv_chain(gpu, M, 5120, 5120, LAYERS, kind="fp8", feed=False)
         g = gpu.graph(step)
         dt = gpu.time_graph(g, reps, 2)
         gbs = gemv_bytes(M, 5120, 5120, 128, kind="fp8") * LAYERS * reps / dt / 1e9
@@ -493,16 +523,23 @@ def decode_step(gpu, Ms, reps, layers=17, hidden=5120, mlp=17408, vocab=152064):
     for _ in range(layers):
         shapes += [(hidden, hidden)] * 4 + [(mlp, hidden), (mlp, hidden), (hidden, mlp)]
     shapes.append((vocab, hidden))
-    ws = [gpu.fp4_layers(1, N, K, 1, seed0=2000 + i)[0] for i, (N, K) in enumerate(shapes)]
+    # weight_scale_2 = 1 / (rms weight * sqrt(K)) keeps the chained
+    # activations near unit scale through all 120 launches (the rms of an
+    # E2M1 code times a scale uniform in [2^-4, 4] is about 6.8); the time
+    # does not depend on it.
+    ws = [gpu.fp4_layers(1, N, K, 1, seed0=2000 + i, ws2=1.0 / (6.8 * K ** 0.5))[0]
+          for i, (N, K) in enumerate(shapes)]
     res = {}
     for M in Ms:
+        # The step's input (never written) and two buffers per width.
         x_h = gpu.t(wl.gen_activation(M, hidden, 1, 11).view(np.int16), torch.bfloat16)
-        bufs = {hidden: [x_h, torch.empty(M, hidden, dtype=torch.bfloat16, device=gpu.dev)],
+        bufs = {hidden: [torch.empty(M, hidden, dtype=torch.bfloat16, device=gpu.dev)
+                         for _ in range(2)],
                 mlp: [torch.empty(M, mlp, dtype=torch.bfloat16, device=gpu.dev) for _ in range(2)],
                 vocab: [torch.empty(M, vocab, dtype=torch.bfloat16, device=gpu.dev)]}
 
         def step():
-            cur = bufs[hidden][0]
+            cur = x_h
             for i, ((N, K), ly) in enumerate(zip(shapes, ws)):
                 y = bufs[N][i % len(bufs[N])]
                 if y is cur:

@@ -60,7 +60,11 @@ namespace {
 
 constexpr int kBM = 128;       // weight rows per tile (MMA M)
 constexpr int kBK = 64;        // k per stage
-constexpr int kDecWarps = 16;  // four per TMEM lane quarter, taking the stages in turn
+// Decoder warps per TMEM lane quarter, each taking every kPh-th stage (kPh
+// stages in flight per quarter).  Measured at M = 8192 (TFLOP/s gate/up /
+// down): 4 -> 1425 / 1516, 5 -> 1397 / 1503, 6 -> 1405 / 1522.
+constexpr int kPh = 4;
+constexpr int kDecWarps = 4 * kPh;
 constexpr int kThreads = (2 + kDecWarps) * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;     // accumulator: columns [0, BN)
@@ -93,7 +97,9 @@ struct GemmCfg {
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int total = abort_flag + 4;
   static constexpr int smem_bytes = total + 1024;  // + alignment slack
-  static_assert(stages >= 4, "ring depth");
+  // A decoder warp's first stage must lie in the ring's first lap: a parity
+  // wait that is a whole lap ahead would match the previous phase.
+  static_assert(stages >= kPh, "ring depth");
   static_assert(a_col + stages * (kBK / 2) <= kTmemCols, "TMEM columns");
   static_assert(smem_bytes <= 227 * 1024, "shared memory");
   // The Y staging tile [BN x 128] and the split-K receive slots (at most 3 x
@@ -431,14 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     uint32_t scn[4];
-    fetch(j4, scn);
+    fetch(j4, scn);  // (j4 = this warp's stage phase, 0 .. kPh - 1)
     bool ok = true;
-    for (int it = j4; it < num_k; it += 4) {
+    for (int it = j4; it < num_k; it += kPh) {
       const int s = it % kStages;
       uint32_t sc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) sc[c] = scn[c];
-      fetch(it + 4, scn);
+      fetch(it + kPh, scn);
       if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) {
         ok = false;
         break;
@@ -483,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[s]);  // one arrival per lane quarter
     }
-    // Epilogue: this warp's lane quarter, token columns [BN/4 j4, BN/4 (j4 + 1)).
+    // Epilogue: this warp's lane quarter, token-column chunks j4, j4 + kPh, ...
     // With a tensor map for Y the tile is staged transposed, [BN tokens x
     // 128 n], in the (now idle) activation ring and written by one tensor
     // store; otherwise each column is stored directly (lanes = consecutive n).
@@ -493,10 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
       uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + L::act);
-      constexpr int kCW = BN / 4;                    // columns of this warp
-      constexpr int kCh = kCW < 32 ? kCW : 32;       // columns per tensor-memory load
+      constexpr int kCh = BN / 4 < 32 ? BN / 4 : 32;  // columns per tensor-memory load
 #pragma unroll 1
-      for (int c0 = kCW * j4; c0 < kCW * j4 + kCW; c0 += kCh) {
+      for (int c0 = kCh * j4; c0 < BN; c0 += kCh * kPh) {
         uint32_t r[kCh];
         tmem_ld_cols<kCh>(lane_base + kAccCol + c0, r);
         if (y_tma) {
@@ -552,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bb == rank) continue;
         const int c_lo = block_lo(bb), w = block_lo(bb + 1) - c_lo;
         const int slot = rank < bb ? rank : rank - 1;
-        // This warp: the block's 8-column chunks j4, j4 + 4, ...
-        for (int c8 = 8 * j4; c8 < w; c8 += 32) {
+        // This warp: the block's 8-column chunks j4, j4 + kPh, ...
+        for (int c8 = 8 * j4; c8 < w; c8 += 8 * kPh) {
           uint32_t r[8];
           tmem_ld8(lane_base + kAccCol + c_lo + c8, r);
           const uint32_t remote =
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
       const float bv = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
       const int c_lo = block_lo(rank), w = block_lo(rank + 1) - c_lo;
-      for (int c8 = 8 * j4; c8 < w; c8 += 32) {
+      for (int c8 = 8 * j4; c8 < w; c8 += 8 * kPh) {
         uint32_t r[8];
         tmem_ld8(lane_base + kAccCol + c_lo + c8, r);
         // Rank order: partials of ranks 0 .. C-1, this rank's own in place.

@@ -9,7 +9,8 @@
 //   empty output          -> return, no launch
 //   K == 0                -> Y = bias (or 0)
 //   M <= 8                -> decode GEMV
-//   M <= 32, NVFP4 bs 16, K % 256 == 0 -> decode GEMV (up to four 8-row tiles)
+//   M <= 32, NVFP4 bs 16, K % 256 == 0 -> decode GEMV (up to four 8-row tiles;
+//                            25..32 rows of a many-tile weight take the GEMM)
 //   M > 8, GEMM-eligible  -> fused tcgen05 GEMM (weight decoded in the main loop;
 //                            token tile 32 / 64 / 128 / 256 by M)
 //   otherwise             -> decode GEMV, one launch per 8-row group
@@ -121,9 +122,13 @@ int matmul_common(GemvArgs& a, cudaStream_t st) {
   if (a.K == 0) return launch_fill_bias(a.bias, a.Y, a.M, a.N, a.dtype, st);
   if (a.M <= 8) return launch_gemv(a, st);
   // Up to 32 rows the decode GEMV shares each decoded weight across all of
-  // them and stays bound by the weight stream; the 256-token GEMM tile would
-  // leave most of the GPU idle at these sizes.
-  if (a.M <= 32 && gemv_tma_supports(a)) return launch_gemv(a, st);
+  // them and stays bound by the weight stream.  With four 8-row activation
+  // tiles (25..32 rows) and a weight of many row tiles the GEMM's two light
+  // CTAs per SM are faster (N = 17408: 27.7 against 30.6 us; N = 5120: the
+  // GEMV, 14.0 against 16.4 us).
+  if (a.M <= 32 && gemv_tma_supports(a) &&
+      !(a.M > 24 && gemm_supports(a) && gemm_prefers_light(a)))
+    return launch_gemv(a, st);
   if (gemm_supports(a)) return launch_gemm(a, st);
   // Decode GEMV per group of rows (blockIdx.z covers up to 65535 groups).
   const int64_t rows_per_launch = int64_t(8) * 65535;

@@ -60,14 +60,26 @@ namespace {
 
 constexpr int kBM = 128;       // weight rows per tile (MMA M)
 constexpr int kBK = 64;        // k per stage
-// Decoder warps per TMEM lane quarter, each taking every kPh-th stage (kPh
-// stages in flight per quarter).  Measured at M = 8192 (TFLOP/s gate/up /
-// down): 4 -> 1425 / 1516, 5 -> 1397 / 1503, 6 -> 1405 / 1522.
-constexpr int kPh = 4;
-constexpr int kDecWarps = 4 * kPh;
-constexpr int kThreads = (2 + kDecWarps) * 32;
-constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;     // accumulator: columns [0, BN)
+
+// PH = decoder warps per TMEM lane quarter, each taking every PH-th stage (PH
+// stages in flight per quarter).  Two shapes of CTA:
+//   PH = 4  one CTA per SM with all 512 tensor-memory columns (prefill tiles;
+//           measured at M = 8192, TFLOP/s gate/up / down: 4 phases 1425 /
+//           1516, 5 phases 1397 / 1503, 6 phases 1405 / 1522);
+//   PH = 2  two CTAs per SM, 256 columns and about 100 KB of shared memory
+//           each, for the narrow token tiles: there the pace of one CTA's
+//           stage loop, not the SM's MMA or decode throughput, bounds the
+//           time, and a second resident CTA (with a K split) runs another
+//           stage loop beside it.
+template <int PH>
+struct Shape {
+  static constexpr int ctas_per_sm = PH == 2 ? 2 : 1;
+  static constexpr int dec_warps = 4 * PH;
+  static constexpr int threads = (2 + dec_warps) * 32;
+  static constexpr int tmem_cols = 512 / ctas_per_sm;
+  static constexpr int smem_budget = ctas_per_sm == 1 ? 216 * 1024 : 100 * 1024;
+};
 
 // Layout per weight format (KIND 0 = NVFP4, 1 = FP8) and token-tile width BN
 // (the MMA N: 256 for prefill, 128 / 64 / 32 for mid-range M, where a
@@ -76,14 +88,15 @@ constexpr int kAccCol = 0;     // accumulator: columns [0, BN)
 // to cover the tensor-copy latency): a stage is the activation tile [BN x 64
 // k] plus the packed weight tile (4 KB NVFP4, 8 KB FP8) in shared memory and
 // 32 tensor-memory columns of decoded operand.
-template <int KIND, int BN>
+template <int KIND, int BN, int PH>
 struct GemmCfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "token tile");
+  using SH = Shape<PH>;
   static constexpr int act_stage = BN * kBK * 2;
   static constexpr int wstage = KIND == 0 ? kBM * kBK / 2 : kBM * kBK;
   static constexpr int a_col = BN;                         // A stages after the accumulator
-  static constexpr int tmem_stages = (kTmemCols - a_col) / (kBK / 2);
-  static constexpr int smem_stages = (216 * 1024) / (act_stage + wstage);
+  static constexpr int tmem_stages = (SH::tmem_cols - a_col) / (kBK / 2);
+  static constexpr int smem_stages = SH::smem_budget / (act_stage + wstage);
   static constexpr int stages0 = tmem_stages < smem_stages ? tmem_stages : smem_stages;
   static constexpr int stages = stages0 > 12 ? 12 : stages0;
   static constexpr int act = 0;
@@ -99,9 +112,9 @@ struct GemmCfg {
   static constexpr int smem_bytes = total + 1024;  // + alignment slack
   // A decoder warp's first stage must lie in the ring's first lap: a parity
   // wait that is a whole lap ahead would match the previous phase.
-  static_assert(stages >= kPh, "ring depth");
-  static_assert(a_col + stages * (kBK / 2) <= kTmemCols, "TMEM columns");
-  static_assert(smem_bytes <= 227 * 1024, "shared memory");
+  static_assert(stages >= PH, "ring depth");
+  static_assert(a_col + stages * (kBK / 2) <= SH::tmem_cols, "TMEM columns");
+  static_assert(smem_bytes * SH::ctas_per_sm <= 227 * 1024, "shared memory");
   // The Y staging tile [BN x 128] and the split-K receive slots (at most 3 x
   // BN/4 columns x 128 rows of FP32, rounded up to 8 columns) fit in the
   // activation ring.
@@ -301,15 +314,17 @@ __device__ __forceinline__ void decode_fp4_word(uint32_t w, uint32_t sc16, uint3
 
 // KIND 0 = NVFP4 weight, 1 = FP8 weight.  DT 0 = FP16, 1 = BF16.  BN =
 // tokens per tile (MMA N).
-template <int DT, int KIND, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int DT, int KIND, int BN, int PH>
+__global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmY, int y_tma,
                    const uint8_t* __restrict__ ws, const float* __restrict__ gscale,
                    const float* __restrict__ fscale, const uint16_t* __restrict__ bias,
                    uint16_t* __restrict__ Y, int M, int N, int K, int bs, int* err) {
-  using L = GemmCfg<KIND, BN>;
+  using L = GemmCfg<KIND, BN, PH>;
   constexpr int kStages = L::stages;
+  constexpr int kPh = PH;
+  constexpr int kTmemCols = Shape<PH>::tmem_cols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -521,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Make the staged tile visible to the tensor-copy engine, then one
       // elected thread stores it (out-of-range rows and columns are clipped).
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(Shape<PH>::dec_warps * 32) : "memory");
       if (have && warp == 2 && lane == 0) {
         asm volatile(
             "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -617,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DT, int KIND, int BN>
+template <int DT, int KIND, int BN, int PH>
 int launch_t(const GemvArgs& a, cudaStream_t st) {
   const int wbytes_per_stage = (KIND == 0) ? kBK / 2 : kBK;
   CUtensorMap tmA, tmW;
@@ -641,25 +656,27 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
                            BN, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
                 ? 1
                 : 0;
-  using L = GemmCfg<KIND, BN>;
+  using L = GemmCfg<KIND, BN, PH>;
+  using SH = Shape<PH>;
   // The shared-memory opt-in is a per-device function attribute.
   static std::once_flag once[64];
   const int dev = device_info().device;
   if (dev < 0 || dev >= 64) return kCuda;
   std::call_once(once[dev], [] {
-    cudaFuncSetAttribute(gemm_tc_kernel<DT, KIND, BN>,
+    cudaFuncSetAttribute(gemm_tc_kernel<DT, KIND, BN, PH>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
   });
-  // Split-K (cluster of C CTAs along z) when the tiles fill less than half
-  // of the GPU: each rank decodes and multiplies 1/C of K, one CTA per SM.
   const int64_t tiles_n = (a.N + kBM - 1) / kBM, tiles_m = (a.M + BN - 1) / BN;
   const int64_t tiles = tiles_n * tiles_m;
   const int num_k = (int)((a.K + kBK - 1) / kBK);
   const int sms = device_info().sm_count;
+  // Split-K (cluster of C CTAs along z) when the tiles fill less than half
+  // of the resident CTA slots.
+  const int64_t slots = (int64_t)sms * SH::ctas_per_sm;
   int C = 1;
-  if (tiles * 2 <= sms) {
+  if (tiles * 2 <= slots) {
     for (int c = 4; c >= 2; --c) {
-      if (tiles * c <= sms && num_k >= 8 * c) {
+      if (tiles * c <= slots && num_k >= 8 * c) {
         C = c;
         break;
       }
@@ -674,7 +691,7 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
   const dim3 grid((unsigned)tiles_n, (unsigned)tiles_m, (unsigned)C);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(SH::threads, 1, 1);
   cfg.dynamicSmemBytes = L::smem_bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -685,7 +702,7 @@ int launch_t(const GemvArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, gemm_tc_kernel<DT, KIND, BN>, tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale,
+      &cfg, gemm_tc_kernel<DT, KIND, BN, PH>, tmA, tmW, tmY, y_tma, a.ws, a.gscale, a.fscale,
       reinterpret_cast<const uint16_t*>(a.bias), reinterpret_cast<uint16_t*>(a.Y), (int)a.M,
       (int)a.N, (int)a.K, a.bs, device_error_word());
   return e == cudaSuccess ? kOk : kCuda;
@@ -701,24 +718,41 @@ int pick_bn(int64_t M) {
   return 256;
 }
 
+// CTA shape for a narrow token tile: when the tiles alone fill at least half
+// of the SMs, two light CTAs per SM (each with a K split of its own); with
+// fewer tiles, one full CTA per SM and a wider K split.  Measured (µs, M = 64
+// / 128): N = 17408 (136 tiles) 36.0 / 36.2 full, 27.9 / 30.5 light; N = 5120
+// (40 tiles) 16.6 / 17.7 full, 16.7 / 19.1 light.
+template <int DT, int KIND, int BN>
+int launch_narrow(const GemvArgs& a, cudaStream_t st) {
+  const int64_t tiles = ((a.N + kBM - 1) / kBM) * ((a.M + BN - 1) / BN);
+  if (tiles * 2 > device_info().sm_count) return launch_t<DT, KIND, BN, 2>(a, st);
+  return launch_t<DT, KIND, BN, 4>(a, st);
+}
+
 template <int DT, int KIND>
 int launch_bn(const GemvArgs& a, cudaStream_t st) {
   switch (pick_bn(a.M)) {
-    case 32: return launch_t<DT, KIND, 32>(a, st);
-    case 64: return launch_t<DT, KIND, 64>(a, st);
-    case 128: return launch_t<DT, KIND, 128>(a, st);
-    default: return launch_t<DT, KIND, 256>(a, st);
+    case 32: return launch_narrow<DT, KIND, 32>(a, st);
+    case 64: return launch_narrow<DT, KIND, 64>(a, st);
+    case 128: return launch_narrow<DT, KIND, 128>(a, st);
+    default: return launch_t<DT, KIND, 256, 4>(a, st);
   }
 }
 
 }  // namespace
 
+bool gemm_prefers_light(const GemvArgs& a) {
+  const int bn = pick_bn(a.M);
+  if (bn > 128) return false;
+  const int64_t tiles = ((a.N + kBM - 1) / kBM) * ((a.M + bn - 1) / bn);
+  return tiles * 2 > device_info().sm_count;
+}
+
 bool gemm_supports(const GemvArgs& a) {
   const DeviceInfo& d = device_info();
   if (d.cc_major != 10) return false;
-  constexpr int kMaxSmem = GemmCfg<1, 256>::smem_bytes > GemmCfg<1, 128>::smem_bytes
-                               ? GemmCfg<1, 256>::smem_bytes
-                               : GemmCfg<1, 128>::smem_bytes;
+  constexpr int kMaxSmem = GemmCfg<1, 256, 4>::smem_bytes;
   if (d.max_smem_optin < kMaxSmem) return false;
   if (a.M <= 8 || a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31)) return false;
   if (a.bs % 16 != 0) return false;

@@ -87,5 +87,8 @@ int launch_nvfp4_qdq_activation(const void* A, void* out, int64_t M, int64_t K, 
 // Returns kUnsupported if the shape cannot take this path.
 int launch_gemm(const GemvArgs& a, cudaStream_t st);
 bool gemm_supports(const GemvArgs& a);
+// The GEMM would run its narrow tile as two light CTAs per SM (the tiles fill
+// at least half of the SMs).
+bool gemm_prefers_light(const GemvArgs& a);
 
 }  // namespace wqmm

@@ -182,3 +182,39 @@ def test_mid_m_gate_up_sampled(M):
     benchmark times it: sampled outputs plus full rows and columns."""
     p = wl.make_fp4(M, 17408, 5120, 16, oracle.BF16, seed=M, bias_sigma=0.02)
     _sampled_check(p, run_fp4, _fp4_sampled, n_random=2048)
+
+
+# --- two light CTAs per SM (narrow tiles whose count fills half the SMs) ---
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+@pytest.mark.parametrize("M,N,K,bs", [
+    (64, 12800, 1024, 16),    # 64-token tile, 100 tiles: K split over 2 ranks
+    (100, 20485, 512, 16),    # 128-token tile, 161 tiles: no split, ragged N
+    (32, 12800, 2080, 32),    # 32-token tile (K % 256 != 0), 100 tiles, split 2
+    (28, 12800, 1024, 16),    # 25..32 rows of a many-tile weight: GEMM, not the GEMV
+])
+def test_light_ctas(M, N, K, bs, dtype):
+    p = wl.make_fp4(M, N, K, bs, dtype, seed=M + N + K, bias_sigma=0.05)
+    assert_within_tolerance(run_fp4(p), *_ref(p), dtype, f"light {M}x{N}x{K}")
+
+
+def test_light_ctas_fp8():
+    p = wl.make_fp8(64, 12800, 1024, 128, oracle.BF16, seed=3, bias_sigma=0.05)
+    Yr, S = oracle.fp8_matmul(p.A, p.B, p.b_scale, p.bias, p.M, p.N, p.K, 128, p.dtype)
+    assert_within_tolerance(run_fp8(p), Yr, S, p.dtype, "fp8 light")
+
+
+def test_one_hot_probe_light_ctas():
+    """Bit-exact one-hot probe through two light CTAs per SM with a K split
+    (M = 64, N = 12800: 100 tiles, 2 ranks)."""
+    M, N, K, bs = 64, 12800, 1024, 16
+    p = wl.make_fp4(M, N, K, bs, oracle.FP16, seed=41, ws2=1.0)
+    d = fp4_dev(p)
+    W = oracle.fp4_dequantize_f64(p.B_packed, p.weight_scale, 1.0, N, K, bs)
+    for shift in (0, 517):
+        ks = (np.arange(M) * 13 + shift) % K
+        A = np.zeros((M, K))
+        A[np.arange(M), ks] = 1.0
+        d["A"] = act_to_dev(wl.act_bits(A, p.dtype), p.dtype)
+        Y = f64_of(run_fp4(p, d))
+        assert np.array_equal(Y, W[:, ks].T), shift

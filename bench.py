@@ -71,10 +71,17 @@ def load_peaks():
                 "src": "fallback"}
 
 
-def csrc_hash():
+# The sources a kernel is built from: its own translation unit (kernel and
+# launcher) and the shared device and host headers.
+KERNEL_SOURCES = {
+    "gemv_decode_M4_N5120_K5120": ("wqmm_gemv.cu", "wqmm_device.cuh", "wqmm_internal.h"),
+}
+
+
+def csrc_hash(files=None):
     d = os.path.join(ROOT, "fp8_weight_only_nvfp4_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files if files is not None else os.listdir(d)):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -82,12 +89,12 @@ def csrc_hash():
 
 def recorded_traffic(kernel_key):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of that kernel (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             rec = json.load(f)
         e = rec.get(kernel_key)
-        if e and e.get("csrc_hash") == csrc_hash():
+        if e and e.get("csrc_hash") == csrc_hash(KERNEL_SOURCES.get(kernel_key)):
             return e.get("dram_bytes_per_launch")
     except Exception:
         pass

@@ -55,7 +55,8 @@ STATUS = {
 SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
            "fp8_quantize_dequantize_activation", "fp4_quantize_activation",
            "fp4_quantize_dequantize_activation", "fp4_dequantize", "fp8_dequantize",
-           "wqmm_status_string", "wqmm_device_status", "wqmm_version")
+           "wqmm_status_string", "wqmm_device_status", "wqmm_selftest_wait_timeout",
+           "wqmm_version")
 
 
 class WqmmError(RuntimeError):
@@ -92,6 +93,7 @@ def lib():
         L.wqmm_status_string.argtypes = [I]
         L.wqmm_status_string.restype = ctypes.c_char_p
         L.wqmm_device_status.argtypes = [P]
+        L.wqmm_selftest_wait_timeout.argtypes = [P]
         L.wqmm_version.argtypes = []
         for name in ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
                      "fp8_quantize_dequantize_activation", "fp4_dequantize",

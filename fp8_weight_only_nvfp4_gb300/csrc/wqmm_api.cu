@@ -18,6 +18,7 @@
 #include <cstring>
 
 #include "../../include/wqmm.h"
+#include "wqmm_device.cuh"
 #include "wqmm_internal.h"
 
 namespace wqmm {
@@ -340,6 +341,25 @@ int wqmm_device_status(void* stream) {
     cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
   }
   return v;
+}
+
+// One warp waits, through the same bounded-wait helper the kernels use, on an
+// mbarrier that nothing arrives on: after the wait limit it records
+// WQMM_ERR_TIMEOUT in the error word and returns.
+__global__ void selftest_wait_kernel(int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  mbar_wait(&bar, 0, err);  // phase 0 never completes
+}
+
+int wqmm_selftest_wait_timeout(void* stream) {
+  if (current_device() < 0) return WQMM_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(device_error_word());
+  return cudaGetLastError() == cudaSuccess ? WQMM_OK : WQMM_ERR_CUDA;
 }
 
 int wqmm_version(void) { return 100; }

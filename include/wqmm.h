@@ -203,6 +203,16 @@ const char* wqmm_status_string(int status);
  */
 int wqmm_device_status(void* stream);
 
+/*
+ * wqmm_selftest_wait_timeout -- diagnostic for the bounded waits: launches one
+ * warp on `stream` that waits, through the same bounded-wait helper as the
+ * kernels, on a barrier that nothing completes.  After the wait limit (2 s)
+ * it records WQMM_ERR_TIMEOUT in the device error word and returns; the CUDA
+ * context stays usable.  Returns WQMM_OK once launched (WQMM_ERR_CUDA if the
+ * launch fails); read the outcome with wqmm_device_status.
+ */
+int wqmm_selftest_wait_timeout(void* stream);
+
 /* Version of this interface (major * 100 + minor). */
 int wqmm_version(void);
 

@@ -701,8 +701,11 @@ int launch_fast_t(const GemvArgs& a, const FastPlan& pl, cudaStream_t st) {
   p.wpc = pl.wpc;
   p.act_pitch = pl.act_pitch;
   p.err = device_error_word();
-  static std::once_flag once[2][2];
-  std::call_once(once[DT][KIND], [] {
+  // The shared-memory opt-in is a per-device function attribute.
+  static std::once_flag once[64];
+  const int dev = device_info().device;
+  if (dev < 0 || dev >= 64) return kCuda;
+  std::call_once(once[dev], [] {
     cudaFuncSetAttribute(gemv_fast<DT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kFastSmemLimit);
   });
@@ -1124,8 +1127,11 @@ int launch_tma_t(const GemvArgs& a, const TmaPlan& pl, cudaStream_t st) {
   p.spc = pl.spc;
   p.nstages = pl.nstages;
   p.err = device_error_word();
-  static std::once_flag once;
-  std::call_once(once, [] {
+  // The shared-memory opt-in is a per-device function attribute.
+  static std::once_flag once[64];
+  const int dev = device_info().device;
+  if (dev < 0 || dev >= 64) return kCuda;
+  std::call_once(once[dev], [] {
     cudaFuncSetAttribute(gemv_tma<DT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kFastSmemLimit);
   });

@@ -437,7 +437,32 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
     const float* fs_row = fscale + (int64_t)n * S;
     // Raw scales of the four 16-k chunks of stage `it` (bs is a multiple of
     // 16), fetched one turn (four stages) ahead of their use.
+    // With 16-element blocks and a scale row length that is a multiple of 4,
+    // a stage's four scale bytes are one aligned word, all of it in range.
+    const bool scale_word = KIND == 0 && bs == 16 && (S & 3) == 0;
+    // FP8 with blocks of 64 or more k: one scale for the whole stage.
+    const bool scale_one = KIND == 1 && (bs & 63) == 0;
     auto fetch = [&](int it, uint32_t (&r)[4]) {
+      if (scale_one) {
+        const int k0 = (k_lo + it) * kBK;
+        uint32_t v = 0u;
+        if (n < N && it < num_k && k0 < K) {
+          const int col = bs_shift >= 0 ? k0 >> bs_shift : k0 / bs;
+          v = __float_as_uint(__ldg(fs_row + col));
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) r[c] = v;
+        return;
+      }
+      if (scale_word) {
+        const int k0 = (k_lo + it) * kBK;
+        uint32_t w = 0u;
+        if (n < N && it < num_k && k0 < K)
+          w = __ldg(reinterpret_cast<const uint32_t*>(ws_row + (k0 >> 4)));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) r[c] = (w >> (8 * c)) & 0xFFu;
+        return;
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int k1 = (k_lo + it) * kBK + 16 * c;

@@ -399,7 +399,13 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
       for (int it = 0; it < num_k && ok; ++it) {
         const int s = it % kStages;
         const uint32_t par = (it / kStages) & 1;
-        ok = wait_bar(&full[s], par, err, abort_flag) && wait_bar(&afull[s], par, err, abort_flag);
+        // afull[s] implies full[s]: every lane quarter's decoder arrives on it
+        // only after its own wait on full[s] (the activation and weight
+        // copies share that barrier), so the activation tile has landed.
+        // One barrier per turn: this thread's turn sets the pipeline's pace
+        // (without the second wait, 1,492 / 1,566 -> 1,590 / 1,667 TFLOP/s at
+        // M = 8192).
+        ok = wait_bar(&afull[s], par, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t act_addr = smem_u32(smem + L::act + s * L::act_stage);

@@ -218,3 +218,32 @@ def test_one_hot_probe_light_ctas():
         d["A"] = act_to_dev(wl.act_bits(A, p.dtype), p.dtype)
         Y = f64_of(run_fp4(p, d))
         assert np.array_equal(Y, W[:, ks].T), shift
+
+
+@pytest.mark.parametrize("kind,M,N,K,bs", [
+    ("fp4", 8192, 17408, 5120, 16),   # the prefill launch: full CTAs, 256-token tiles
+    ("fp4", 64, 17408, 5120, 16),     # two light CTAs per SM, K split over 2
+    ("fp4", 256, 640, 5120, 16),      # full CTAs, K split over 4
+    ("fp8", 8192, 5120, 4096, 128),   # FP8 prefill
+])
+def test_gemm_repeated_runs_bit_identical(kind, M, N, K, bs):
+    """Ten runs into fresh output buffers give the same bits: the stage ring
+    hands every stage to the MMA only after its copies have landed and its
+    operand is stored (a stage read early or overwritten late would show up
+    as run-to-run differences)."""
+    import torch
+    if kind == "fp4":
+        p = wl.make_fp4(8, N, K, bs, oracle.BF16, seed=N + K, bias_sigma=0.02)
+        d = fp4_dev(p)
+        d["A"] = torch.randn(M, K, device="cuda:0", dtype=torch.bfloat16)
+        run = lambda: run_fp4(p, d)
+    else:
+        p = wl.make_fp8(8, N, K, bs, oracle.BF16, seed=N + K, bias_sigma=0.02)
+        from gpu_util import fp8_dev
+        d = fp8_dev(p)
+        d["A"] = torch.randn(M, K, device="cuda:0", dtype=torch.bfloat16)
+        run = lambda: run_fp8(p, d)
+    first = run()
+    assert torch.isfinite(first.float()).all()
+    for _ in range(9):
+        assert torch.equal(run(), first)

@@ -396,28 +396,42 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
       constexpr uint32_t idesc = make_idesc<BN>(DT == 1 ? 1 : 0);
       bool ok = true;
       int committed = -1;
-      for (int it = 0; it < num_k && ok; ++it) {
-        const int s = it % kStages;
-        const uint32_t par = (it / kStages) & 1;
+      // Stage, parity, operand descriptor and tensor-memory address advance
+      // by counters: this thread's turn sets the pipeline's pace, so it does
+      // as little as possible.
+      const uint64_t bdesc0 = desc_kmajor_sw128(smem_u32(smem + L::act));
+      const uint32_t afull0 = smem_u32(afull);
+      uint64_t bdesc = bdesc0;
+      uint32_t a_tmem = tmem + L::a_col;
+      int s = 0;
+      uint32_t par = 0;
+      for (int it = 0; it < num_k; ++it) {
         // afull[s] implies full[s]: every lane quarter's decoder arrives on it
         // only after its own wait on full[s] (the activation and weight
         // copies share that barrier), so the activation tile has landed.
-        // One barrier per turn: this thread's turn sets the pipeline's pace
-        // (without the second wait, 1,492 / 1,566 -> 1,590 / 1,667 TFLOP/s at
-        // M = 8192).
-        ok = wait_bar(&afull[s], par, err, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t act_addr = smem_u32(smem + L::act + s * L::act_stage);
-        const uint64_t bdesc = desc_kmajor_sw128(act_addr);
-#pragma unroll
-        for (int j = 0; j < kBK / 16; ++j) {
-          const uint32_t a_tmem = tmem + L::a_col + s * (kBK / 2) + j * 8;
-          mma_ts(tmem + kAccCol, a_tmem, bdesc + (uint64_t)((j * 32) >> 4), idesc,
-                 (it > 0 || j > 0) ? 1u : 0u);
+        // One barrier per turn (without the second wait, 1,492 / 1,566 ->
+        // 1,590 / 1,667 TFLOP/s at M = 8192).
+        if (!mbar_try_wait(afull0 + 8u * (uint32_t)s, par) &&
+            !wait_bar(&afull[s], par, err, abort_flag)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < kBK / 16; ++j)
+          mma_ts(tmem + kAccCol, a_tmem + j * 8, bdesc + (uint64_t)((j * 32) >> 4), idesc,
+                 (it > 0 || j > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
         committed = it;
+        if (++s == kStages) {
+          s = 0;
+          par ^= 1u;
+          bdesc = bdesc0;
+          a_tmem = tmem + L::a_col;
+        } else {
+          bdesc += (uint64_t)(L::act_stage >> 4);
+          a_tmem += kBK / 2;
+        }
       }
       if (ok) {
         mma_commit(accfull);

@@ -64,9 +64,8 @@ constexpr int kAccCol = 0;     // accumulator: columns [0, BN)
 
 // PH = decoder warps per TMEM lane quarter, each taking every PH-th stage (PH
 // stages in flight per quarter).  Two shapes of CTA:
-//   PH = 4  one CTA per SM with all 512 tensor-memory columns (prefill tiles;
-//           measured at M = 8192, TFLOP/s gate/up / down: 4 phases 1425 /
-//           1516, 5 phases 1397 / 1503, 6 phases 1405 / 1522);
+//   PH >= 3 one CTA per SM with all 512 tensor-memory columns (prefill tiles,
+//           and narrow tiles when the tiles are few);
 //   PH = 2  two CTAs per SM, 256 columns and about 100 KB of shared memory
 //           each, for the narrow token tiles: there the pace of one CTA's
 //           stage loop, not the SM's MMA or decode throughput, bounds the
@@ -98,7 +97,14 @@ struct GemmCfg {
   static constexpr int tmem_stages = (SH::tmem_cols - a_col) / (kBK / 2);
   static constexpr int smem_stages = SH::smem_budget / (act_stage + wstage);
   static constexpr int stages0 = tmem_stages < smem_stages ? tmem_stages : smem_stages;
-  static constexpr int stages = stages0 > 12 ? 12 : stages0;
+  static constexpr int stages1 = stages0 > 12 ? 12 : stages0;
+  // A whole number of turns: a decoder warp waits on a stage's barrier by
+  // parity, which is only safe if that barrier's previous phase (the slot's
+  // previous fill) has completed.  With stages % PH == 0 the slot's previous
+  // fill is this same warp's previous stage, whose wait it has passed; with
+  // any other depth it belongs to another warp, and a copy landing out of
+  // order would let the wait match the phase two fills back.
+  static constexpr int stages = stages1 / PH * PH;
   static constexpr int act = 0;
   static constexpr int w = act + stages * act_stage;
   static constexpr int bars = w + stages * wstage;
@@ -110,9 +116,7 @@ struct GemmCfg {
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int total = abort_flag + 4;
   static constexpr int smem_bytes = total + 1024;  // + alignment slack
-  // A decoder warp's first stage must lie in the ring's first lap: a parity
-  // wait that is a whole lap ahead would match the previous phase.
-  static_assert(stages >= PH, "ring depth");
+  static_assert(stages >= PH && stages % PH == 0, "ring depth");
   static_assert(a_col + stages * (kBK / 2) <= SH::tmem_cols, "TMEM columns");
   static_assert(smem_bytes * SH::ctas_per_sm <= 227 * 1024, "shared memory");
   // The Y staging tile [BN x 128] and the split-K receive slots (at most 3 x
@@ -763,6 +767,14 @@ int pick_bn(int64_t M) {
   return 256;
 }
 
+// Decoder phases of the full CTA at the 256-token tile, per weight format:
+// the ring depth is the largest multiple of the phase count that fits, so
+// the counts that divide the deepest rings (6 stages NVFP4, 5 FP8) keep them.
+// Measured at M = 8192 (TFLOP/s gate/up / down, FP8): 3 phases x 6 stages
+// 1,606 / 1,666; 6 x 6 1,598 / 1,673; 4 x 4 1,549 / 1,472; FP8 5 x 5 1,380,
+// 4 x 4 1,135.
+constexpr int kFullPh256[2] = {3, 5};
+
 // CTA shape for a narrow token tile: when the tiles alone fill at least half
 // of the SMs, two light CTAs per SM (each with a K split of its own); with
 // fewer tiles, one full CTA per SM and a wider K split.  Measured (µs, M = 64
@@ -781,7 +793,7 @@ int launch_bn(const GemvArgs& a, cudaStream_t st) {
     case 32: return launch_narrow<DT, KIND, 32>(a, st);
     case 64: return launch_narrow<DT, KIND, 64>(a, st);
     case 128: return launch_narrow<DT, KIND, 128>(a, st);
-    default: return launch_t<DT, KIND, 256, 4>(a, st);
+    default: return launch_t<DT, KIND, 256, kFullPh256[KIND]>(a, st);
   }
 }
 

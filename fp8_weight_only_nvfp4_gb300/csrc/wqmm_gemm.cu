@@ -13,21 +13,22 @@
 //
 // Tile: 128 weight rows (MMA M) x BN tokens (MMA N) per CTA, K in stages of
 // 64; BN = 256 for prefill, 128 / 64 / 32 when M fits a narrower tile.
-// Roles (one CTA = 18 warps):
+// Roles (one CTA = 2 + 4 PH warps, PH = decoder phases, see Shape below):
 //   warp 0     TMA producer: activation tile [BN tokens x 64 k] (128-byte
 //              swizzle, K-major) and packed weight tile [128 rows x 64 k]
 //              into a shared-memory ring (6 stages for NVFP4 and 5 for FP8
-//              at BN = 256, up to 12 for narrower tiles);
+//              at BN = 256, up to 12 for narrower tiles; always a multiple
+//              of PH);
 //   warp 1     TMEM owner and MMA issuer (one elected thread):
 //              tcgen05.mma.kind::f16, A = decoded weight from TMEM,
 //              B = activation tile from shared memory, D = FP32 in TMEM;
-//   warps 2-17 decoders: warp w serves TMEM lane quarter (w % 4) and decodes
-//              every fourth stage in full; thread i of the quarter owns
+//   warps 2..  decoders: warp w serves TMEM lane quarter (w % 4) and decodes
+//              every PH-th stage in full; thread i of the quarter owns
 //              weight row i (TMEM lane i).  It reads its packed bytes from
 //              shared memory, folds the E4M3 block scales (exact for NVFP4:
 //              <= 6 significant bits, FP4 page §4), writes the 16-bit
 //              operands to TMEM with one tcgen05.st, and after the main loop
-//              runs the epilogue for a quarter of the BN token columns: TMEM
+//              runs the epilogue for its share of the BN token columns: TMEM
 //              -> registers, * gscale, + bias, one RNE, then Y (through a
 //              shared-memory transpose and one tensor store when the row
 //              pitch allows, else direct stores with lanes = consecutive n).
@@ -38,8 +39,8 @@
 //              token-column block b and adds the partials in rank order).
 //              Measured: without the tensor-memory stores the kernel runs at
 //              the speed of the plain MMA pipeline; the stores complete late
-//              while the MMA streams, so the four warps of a quarter keep
-//              four stages in flight instead of splitting one stage's k.
+//              while the MMA streams, so the PH warps of a quarter keep PH
+//              stages in flight instead of splitting one stage's k.
 //
 // The weight being the MMA A operand is the FP4 page §4 idea (weight in the
 // A slot, activation in the B slot) carried to tcgen05: the decoded weight
@@ -446,11 +447,13 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
     }
   } else {
     // ---------------- decoders, then epilogue ----------------
-    // Warp w serves TMEM lane quarter q = w % 4 and decodes every fourth
-    // stage (phase j = (w - 2) / 4) in full: the four warps of a quarter
-    // have four stages in flight, so the latency of one warp's stage
-    // (shared load, decode, tensor-memory store, which completes late while
-    // the MMA streams) is spread over four stages.
+    // Warp w serves TMEM lane quarter q = w % 4 and decodes every PH-th
+    // stage (phase j = (w - 2) / 4) in full: the PH warps of a quarter have
+    // PH stages in flight, so the latency of one warp's stage (shared load,
+    // decode, tensor-memory store, which completes late while the MMA
+    // streams) is spread over PH stages.  The ring depth is a multiple of
+    // PH, so a warp's parity wait on a slot always follows its own wait on
+    // the slot's previous fill.
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int j4 = (warp - 2) >> 2;         // stage phase of this warp
     const int row = q * 32 + lane;          // weight row within the tile

@@ -149,12 +149,21 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16, single CTA.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16, single CTA, for one 64-k
+// stage: four K=16 MMAs into D, A stepping 8 tensor-memory columns
+// and B 32 bytes (2 descriptor units) per MMA; the first accumulates only if
+// `accumulate`, the others always.
+__device__ __forceinline__ void mma_ts_stage(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+      "{ .reg .pred p, t; .reg .b32 a1, a2, a3; .reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0; setp.eq.b32 t, %3, %3;\n\t"
+      "add.u32 a1, %1, 8; add.u32 a2, %1, 16; add.u32 a3, %1, 24;\n\t"
+      "add.u64 b1, %2, 2; add.u64 b2, %2, 4; add.u64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t; }" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -422,10 +431,8 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
           break;
         }
         tc_fence_after();
-#pragma unroll
-        for (int j = 0; j < kBK / 16; ++j)
-          mma_ts(tmem + kAccCol, a_tmem + j * 8, bdesc + (uint64_t)((j * 32) >> 4), idesc,
-                 (it > 0 || j > 0) ? 1u : 0u);
+        static_assert(kBK == 64, "four MMAs of K = 16 per stage");
+        mma_ts_stage(tmem + kAccCol, a_tmem, bdesc, idesc, it > 0 ? 1u : 0u);
         mma_commit(&empty[s]);
         committed = it;
         if (++s == kStages) {

@@ -72,9 +72,13 @@ typedef enum {
  *   block_size     K elements per scale; must be a positive multiple of 16.
  *
  * Paths: M <= 8 runs the decode GEMV (each weight byte read once, the decode
- * shared by all M rows); larger M with K % 32 == 0 runs the fused tcgen05
- * GEMM (the weight is dequantized inside the main loop, no [N, K] scratch);
- * other shapes run the GEMV once per 8-row group of A.
+ * shared by all M rows), and so does M <= 32 when block_size == 16 and
+ * K % 256 == 0 (up to four 8-row activation tiles per decoded weight
+ * fragment), except 25..32 rows of a weight with many 128-row tiles; larger M
+ * with K % 32 == 0 runs the fused tcgen05 GEMM (the weight is dequantized
+ * inside the main loop, no [N, K] scratch; a 32/64/128/256-token tile by M);
+ * other shapes run the GEMV once per 8-row group of A.  All paths meet the
+ * accuracy bound below; which one runs changes only the summation order.
  * Errors: odd K or block_size < 1 -> INVALID_ARG; block_size % 16 != 0 ->
  * UNSUPPORTED; any size < 0 -> INVALID_ARG.
  * Accuracy: |Y - Y_exact| <= 8e-3 * sum_k |A * B_dq| + 1e-3 (BF16) and

@@ -16,7 +16,7 @@
 //         Most Expensive Kernel in H200 Prefill", section "Bitwise equivalence
 //         was checked at three levels" (-0.0 from code 0x8).
 //
-// Readings taken where the pages are silent (each is listed in the design doc):
+// Readings taken where the pages are silent:
 //   * dequant order: (e2m1 * e4m3) in fp32 (exact), then * weight_scale_2 in
 //     fp32 (one RNE rounding), then RNE to the activation type;
 //   * E4M3 scale bytes are the "fn" variant (no infinities, 0x7F/0xFF = NaN);

@@ -125,9 +125,11 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, device):
     torch = _torch()
-    s = torch.cuda.current_stream() if stream is None else stream
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    if s.device != device:
+        raise ValueError(f"stream is on {s.device}, the tensors on {device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -136,49 +138,110 @@ def _check(status: int, where: str):
         raise WqmmError(status, where)
 
 
-def _need_cuda(*ts):
-    for t in ts:
-        if t is not None:
-            if not t.is_cuda:
-                raise ValueError("all tensors must be CUDA tensors (no CPU fallback)")
-            if not t.is_contiguous():
-                raise ValueError("all tensors must be contiguous")
+def _need(t, name, device, dtypes=None, shape=None, numel=None):
+    """Validate one tensor argument before its address reaches the library:
+    a CUDA tensor on `device`, contiguous, of one of `dtypes`, with exactly
+    `shape` (or `numel` elements).  A wrong shape or dtype would make the
+    kernels read or write outside the buffer, so nothing is passed on."""
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU fallback)")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, A on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype {' or '.join(str(d) for d in dtypes)}, "
+                         f"got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
 
 
-def _need_scale(a_scale):
-    if a_scale.dtype != _torch().float32 or a_scale.numel() != 1:
-        raise ValueError("a_scale must be a one-element float32 tensor")
+def _act_dtypes():
+    torch = _torch()
+    return (torch.float16, torch.bfloat16)
+
+
+def _byte_dtypes():
+    torch = _torch()
+    d = [torch.uint8]
+    if hasattr(torch, "float8_e4m3fn"):
+        d.append(torch.float8_e4m3fn)
+    return tuple(d)
+
+
+def _device_of(A):
+    if not A.is_cuda:
+        raise ValueError("A must be a CUDA tensor (there is no CPU fallback)")
+    return A.device
+
+
+def _scale_cols(K, block_size):
+    if int(block_size) < 1:
+        raise ValueError(f"block_size must be >= 1, got {block_size}")
+    return (K + int(block_size) - 1) // int(block_size)
+
+
+def _check_a_scale(a_scale, dev):
+    _need(a_scale, "a_scale", dev, (_torch().float32,), numel=1)
 
 
 def fp4_weight_matmul(A, B_packed, weight_scale, weight_scale_2, bias=None, block_size=16,
                       out=None, stream=None):
     torch = _torch()
-    _need_cuda(A, B_packed, weight_scale, weight_scale_2, bias, out)
+    dev = _device_of(A)
+    _need(A, "A", dev, _act_dtypes())
+    if B_packed.dim() != 2:
+        raise ValueError(f"B_packed must be 2-D [N, K/2], got shape {tuple(B_packed.shape)}")
     N = B_packed.shape[0]
     K = 2 * B_packed.shape[1]
-    if A.shape[-1] != K:
-        raise ValueError(f"A.shape[-1]={A.shape[-1]} != K={K}")
+    if A.dim() < 1 or A.shape[-1] != K:
+        raise ValueError(f"A.shape[-1]={A.shape[-1] if A.dim() else None} != K={K}")
+    S = _scale_cols(K, block_size)
+    _need(B_packed, "B_packed", dev, (torch.uint8,))
+    _need(weight_scale, "weight_scale", dev, _byte_dtypes(), shape=(N, S))
+    _need(weight_scale_2, "weight_scale_2", dev, (torch.float32,), numel=1)
+    _need(bias, "bias", dev, (A.dtype,), numel=N)
     M = A.numel() // K if K else int(torch.tensor(A.shape[:-1]).prod())
     if out is None:
-        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=A.device)
-    st = lib().fp4_weight_matmul(_ptr(A), _ptr(B_packed), _ptr(weight_scale),
-                                 _ptr(weight_scale_2), _ptr(bias), _ptr(out), M, N, K,
-                                 int(block_size), _dt(A.dtype), _stream(stream))
+        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=dev)
+    _need(out, "out", dev, (A.dtype,), shape=tuple(A.shape[:-1]) + (N,))
+    with torch.cuda.device(dev):
+        st = lib().fp4_weight_matmul(_ptr(A), _ptr(B_packed), _ptr(weight_scale),
+                                     _ptr(weight_scale_2), _ptr(bias), _ptr(out), M, N, K,
+                                     int(block_size), _dt(A.dtype), _stream(stream, dev))
     _check(st, "fp4_weight_matmul")
     return out
 
 
-def fp8_weight_matmul(A, B, b_scale, bias=None, block_size=128, out=None, stream=None):
+def _fp8_common(A, B, b_scale, bias, block_size, out):
     torch = _torch()
-    _need_cuda(A, B, b_scale, bias, out)
+    dev = _device_of(A)
+    _need(A, "A", dev, _act_dtypes())
+    if B.dim() != 2:
+        raise ValueError(f"B must be 2-D [N, K], got shape {tuple(B.shape)}")
     N, K = B.shape
-    if A.shape[-1] != K:
-        raise ValueError(f"A.shape[-1]={A.shape[-1]} != K={K}")
+    if A.dim() < 1 or A.shape[-1] != K:
+        raise ValueError(f"A.shape[-1]={A.shape[-1] if A.dim() else None} != K={K}")
+    _need(B, "B", dev, _byte_dtypes())
+    _need(b_scale, "b_scale", dev, (torch.float32,), shape=(N, _scale_cols(K, block_size)))
+    _need(bias, "bias", dev, (A.dtype,), numel=N)
     M = A.numel() // K if K else int(torch.tensor(A.shape[:-1]).prod())
     if out is None:
-        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=A.device)
-    st = lib().fp8_weight_matmul(_ptr(A), _ptr(B), _ptr(b_scale), _ptr(bias), _ptr(out), M, N,
-                                 K, int(block_size), _dt(A.dtype), _stream(stream))
+        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=dev)
+    _need(out, "out", dev, (A.dtype,), shape=tuple(A.shape[:-1]) + (N,))
+    return dev, M, N, K, out
+
+
+def fp8_weight_matmul(A, B, b_scale, bias=None, block_size=128, out=None, stream=None):
+    torch = _torch()
+    dev, M, N, K, out = _fp8_common(A, B, b_scale, bias, block_size, out)
+    with torch.cuda.device(dev):
+        st = lib().fp8_weight_matmul(_ptr(A), _ptr(B), _ptr(b_scale), _ptr(bias), _ptr(out), M,
+                                     N, K, int(block_size), _dt(A.dtype), _stream(stream, dev))
     _check(st, "fp8_weight_matmul")
     return out
 
@@ -188,35 +251,36 @@ def fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias=None, block_size=128, ou
     """FP8 page §6 W8A8 path: Y = (fp8_e4m3(A / a_scale) * a_scale) * dequant(B)^T (+ bias).
     a_scale is a one-element float32 CUDA tensor."""
     torch = _torch()
-    _need_cuda(A, a_scale, B, b_scale, bias, out)
-    _need_scale(a_scale)
-    N, K = B.shape
-    if A.shape[-1] != K:
-        raise ValueError(f"A.shape[-1]={A.shape[-1]} != K={K}")
-    M = A.numel() // K if K else int(torch.tensor(A.shape[:-1]).prod())
-    if out is None:
-        out = torch.empty(*A.shape[:-1], N, dtype=A.dtype, device=A.device)
-    st = lib().fp8_weight_matmul_w8a8(_ptr(A), _ptr(a_scale), _ptr(B), _ptr(b_scale), _ptr(bias),
-                                      _ptr(out), M, N, K, int(block_size), _dt(A.dtype),
-                                      _stream(stream))
+    dev, M, N, K, out = _fp8_common(A, B, b_scale, bias, block_size, out)
+    _check_a_scale(a_scale, dev)
+    with torch.cuda.device(dev):
+        st = lib().fp8_weight_matmul_w8a8(_ptr(A), _ptr(a_scale), _ptr(B), _ptr(b_scale),
+                                          _ptr(bias), _ptr(out), M, N, K, int(block_size),
+                                          _dt(A.dtype), _stream(stream, dev))
     _check(st, "fp8_weight_matmul_w8a8")
     return out
 
 
 def fp8_quantize_dequantize_activation(A, a_scale, out=None, stream=None):
     """A_deq = fp8_e4m3(A / a_scale) * a_scale, elementwise (bit-exact contract)."""
-    _need_cuda(A, a_scale, out)
-    _need_scale(a_scale)
     torch = _torch()
+    dev = _device_of(A)
+    _need(A, "A", dev, _act_dtypes())
+    _check_a_scale(a_scale, dev)
     if out is None:
         out = torch.empty_like(A)
-    st = lib().fp8_quantize_dequantize_activation(_ptr(A), _ptr(a_scale), _ptr(out), A.numel(),
-                                                  _dt(A.dtype), _stream(stream))
+    _need(out, "out", dev, (A.dtype,), numel=A.numel())
+    with torch.cuda.device(dev):
+        st = lib().fp8_quantize_dequantize_activation(_ptr(A), _ptr(a_scale), _ptr(out),
+                                                      A.numel(), _dt(A.dtype),
+                                                      _stream(stream, dev))
     _check(st, "fp8_quantize_dequantize_activation")
     return out
 
 
 def _rows_k(A):
+    if A.dim() < 1:
+        raise ValueError("A must have at least one dimension")
     K = A.shape[-1]
     return A.numel() // K if K else 0, K
 
@@ -225,15 +289,21 @@ def fp4_quantize_activation(A, out_packed=None, out_scale=None, stream=None):
     """NVFP4 quantization of an activation (FP4 page §6, step 1): returns
     (A_packed [..., K/2] uint8, A_scale [..., ceil(K/16)] uint8 E4M3)."""
     torch = _torch()
-    _need_cuda(A, out_packed, out_scale)
+    dev = _device_of(A)
+    _need(A, "A", dev, _act_dtypes())
     M, K = _rows_k(A)
     lead = tuple(A.shape[:-1])
+    if K % 2:
+        raise ValueError(f"K={K} must be even (two codes per byte)")
     if out_packed is None:
-        out_packed = torch.empty(lead + (K // 2,), dtype=torch.uint8, device=A.device)
+        out_packed = torch.empty(lead + (K // 2,), dtype=torch.uint8, device=dev)
     if out_scale is None:
-        out_scale = torch.empty(lead + ((K + 15) // 16,), dtype=torch.uint8, device=A.device)
-    st = lib().fp4_quantize_activation(_ptr(A), _ptr(out_packed), _ptr(out_scale), M, K,
-                                       _dt(A.dtype), _stream(stream))
+        out_scale = torch.empty(lead + ((K + 15) // 16,), dtype=torch.uint8, device=dev)
+    _need(out_packed, "out_packed", dev, (torch.uint8,), shape=lead + (K // 2,))
+    _need(out_scale, "out_scale", dev, _byte_dtypes(), shape=lead + ((K + 15) // 16,))
+    with torch.cuda.device(dev):
+        st = lib().fp4_quantize_activation(_ptr(A), _ptr(out_packed), _ptr(out_scale), M, K,
+                                           _dt(A.dtype), _stream(stream, dev))
     _check(st, "fp4_quantize_activation")
     return out_packed, out_scale
 
@@ -242,12 +312,15 @@ def fp4_quantize_dequantize_activation(A, out=None, stream=None):
     """e2m1(code) * e4m3(scale) of fp4_quantize_activation, in A's dtype
     (exact); feeding it to fp4_weight_matmul gives the FP4 x FP4 numerics."""
     torch = _torch()
-    _need_cuda(A, out)
+    dev = _device_of(A)
+    _need(A, "A", dev, _act_dtypes())
     M, K = _rows_k(A)
     if out is None:
         out = torch.empty_like(A)
-    st = lib().fp4_quantize_dequantize_activation(_ptr(A), _ptr(out), M, K, _dt(A.dtype),
-                                                  _stream(stream))
+    _need(out, "out", dev, (A.dtype,), shape=tuple(A.shape))
+    with torch.cuda.device(dev):
+        st = lib().fp4_quantize_dequantize_activation(_ptr(A), _ptr(out), M, K, _dt(A.dtype),
+                                                      _stream(stream, dev))
     _check(st, "fp4_quantize_dequantize_activation")
     return out
 
@@ -255,31 +328,53 @@ def fp4_quantize_dequantize_activation(A, out=None, stream=None):
 def fp4_dequantize(B_packed, weight_scale, weight_scale_2, block_size=16, dtype=None,
                    out=None, stream=None):
     torch = _torch()
-    _need_cuda(B_packed, weight_scale, weight_scale_2, out)
-    dtype = torch.bfloat16 if dtype is None else dtype
+    dev = _device_of(B_packed)
+    if B_packed.dim() != 2:
+        raise ValueError(f"B_packed must be 2-D [N, K/2], got shape {tuple(B_packed.shape)}")
     N = B_packed.shape[0]
     K = 2 * B_packed.shape[1]
+    _need(B_packed, "B_packed", dev, (torch.uint8,))
+    _need(weight_scale, "weight_scale", dev, _byte_dtypes(),
+          shape=(N, _scale_cols(K, block_size)))
+    _need(weight_scale_2, "weight_scale_2", dev, (torch.float32,), numel=1)
+    dtype = torch.bfloat16 if dtype is None else dtype
     if out is None:
-        out = torch.empty(N, K, dtype=dtype, device=B_packed.device)
-    st = lib().fp4_dequantize(_ptr(B_packed), _ptr(weight_scale), _ptr(weight_scale_2),
-                              _ptr(out), N, K, int(block_size), _dt(out.dtype), _stream(stream))
+        out = torch.empty(N, K, dtype=dtype, device=dev)
+    _need(out, "out", dev, _act_dtypes(), shape=(N, K))
+    with torch.cuda.device(dev):
+        st = lib().fp4_dequantize(_ptr(B_packed), _ptr(weight_scale), _ptr(weight_scale_2),
+                                  _ptr(out), N, K, int(block_size), _dt(out.dtype),
+                                  _stream(stream, dev))
     _check(st, "fp4_dequantize")
     return out
 
 
 def fp8_dequantize(B, b_scale, block_size=128, dtype=None, out=None, stream=None):
     torch = _torch()
-    _need_cuda(B, b_scale, out)
-    dtype = torch.bfloat16 if dtype is None else dtype
+    dev = _device_of(B)
+    if B.dim() != 2:
+        raise ValueError(f"B must be 2-D [N, K], got shape {tuple(B.shape)}")
     N, K = B.shape
+    _need(B, "B", dev, _byte_dtypes())
+    _need(b_scale, "b_scale", dev, (torch.float32,), shape=(N, _scale_cols(K, block_size)))
+    dtype = torch.bfloat16 if dtype is None else dtype
     if out is None:
-        out = torch.empty(N, K, dtype=dtype, device=B.device)
-    st = lib().fp8_dequantize(_ptr(B), _ptr(b_scale), _ptr(out), N, K, int(block_size),
-                              _dt(out.dtype), _stream(stream))
+        out = torch.empty(N, K, dtype=dtype, device=dev)
+    _need(out, "out", dev, _act_dtypes(), shape=(N, K))
+    with torch.cuda.device(dev):
+        st = lib().fp8_dequantize(_ptr(B), _ptr(b_scale), _ptr(out), N, K, int(block_size),
+                                  _dt(out.dtype), _stream(stream, dev))
     _check(st, "fp8_dequantize")
     return out
 
 
-def device_status(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the device error word."""
-    return int(lib().wqmm_device_status(_stream(stream)))
+def device_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word of
+    its device (the current device when neither is given)."""
+    torch = _torch()
+    if device is None:
+        device = stream.device if stream is not None else torch.device(
+            "cuda", torch.cuda.current_device())
+    device = torch.device(device)
+    with torch.cuda.device(device):
+        return int(lib().wqmm_device_status(_stream(stream, device)))

@@ -1,7 +1,8 @@
 // wqmm_actq.cu -- NVFP4 activation quantization: step 1 of the native FP4 x
 // FP4 path of "MatMulBlockQuantizedFp4Weight - CUDA Operator Documentation"
-// §6 ("quantize activation A to packed NVFP4 E2M1 with per-16-block E4M3
-// scales").  The page gives no formula; per 16-element block of a row:
+// §6, which brings the activation into the weight's format (two E2M1 codes
+// per byte, one E4M3 scale per 16 elements).  The page gives no formula; per
+// 16-element block of a row:
 //
 //   amax  = max |a|                      (a exact in float32)
 //   scale = E4M3(fp32(amax / 6))         RNE, saturating at 448

@@ -179,6 +179,10 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t ra
   return r;
 }
 
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float a, float b, float c,
                                                  float d) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
@@ -219,6 +223,20 @@ __device__ __forceinline__ void ldg_stream_v8(const void* p, uint32_t (&r)[8]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7])
       : "l"(p));
+}
+
+// Coherent (L2) loads for data another kernel may have just written: no
+// read-only or L1 caching.
+__device__ __forceinline__ float ld_global_f32(const float* p) {
+  float r;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t ld_global_u16(const uint16_t* p) {
+  uint16_t r;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
 }
 
 __device__ __forceinline__ void stg_v4(void* p, uint4 v) {

@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool have = false;  // decoder warps: this CTA's accumulator is complete
+  // FP8 weights with FP16 activations: 2^E of this decoder thread's weight
+  // row, by which its accumulator is multiplied back (1 otherwise).
+  float row_pow2 = 1.0f;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -510,6 +513,29 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
         }
       }
     };
+    // FP8 weights with FP16 activations: the folded operand e4m3 * b_scale
+    // has to stay inside the FP16 range whatever b_scale is (448 * 147
+    // already overflows it).  A decoder thread owns one weight row over the
+    // CTA's whole K range, so it divides that row's block scales by the
+    // power of two 2^E that brings their largest magnitude into [1, 2) --
+    // exact -- and its accumulator is multiplied by 2^E afterwards, also
+    // exact: every operand then lies within 448 * 2.
+    float scale_norm = 1.0f;
+    if constexpr (KIND == 1 && DT == 0) {
+      float rmax = 0.f;
+      if (n < N) {
+        const int k_begin = k_lo * kBK, k_end = min(K, (k_lo + num_k) * kBK);
+        const int c0 = bs_shift >= 0 ? k_begin >> bs_shift : k_begin / bs;
+        const int c1 = bs_shift >= 0 ? (k_end - 1) >> bs_shift : (k_end - 1) / bs;
+        for (int c = c0; c <= c1; ++c) rmax = fmaxf(rmax, fabsf(__ldg(fs_row + c)));
+      }
+      // floor(log2(rmax)) for a normal rmax; zero, subnormal, inf and NaN
+      // maxima keep E = 0.
+      const int e = (int)((__float_as_uint(rmax) >> 23) & 0xFFu) - 127;
+      const int ec = (e >= -126 && e <= 126) ? e : 0;
+      scale_norm = __uint_as_float((uint32_t)(127 - ec) << 23);
+      row_pow2 = __uint_as_float((uint32_t)(127 + ec) << 23);
+    }
     uint32_t scn[4];
     fetch(j4, scn);  // (j4 = this warp's stage phase, 0 .. kPh - 1)
     bool ok = true;
@@ -546,7 +572,8 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
         for (int c = 0; c < 4; ++c) {
           const uint4 p = lds_swz<3>(wt, row * 64 + 16 * c);
           const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
-          const float scf = __uint_as_float(sc[c]);
+          float scf = __uint_as_float(sc[c]);
+          if constexpr (DT == 0) scf *= scale_norm;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -567,10 +594,10 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
     // With a tensor map for Y the tile is staged transposed, [BN tokens x
     // 128 n], in the (now idle) activation ring and written by one tensor
     // store; otherwise each column is stored directly (lanes = consecutive n).
-    have = ok && wait_bar(accfull, 0, err, abort_flag);
+    have = ok && wait_bar(accfull, 0, err, abort_flag) && !*abort_flag;
     if (have && C == 1) {
       tc_fence_after();
-      const float gs = (KIND == 0) ? __ldg(gscale) : 1.0f;
+      const float gs = (KIND == 0) ? __ldg(gscale) : row_pow2;
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
       uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + L::act);
       constexpr int kCh = BN / 4 < 32 ? BN / 4 : 32;  // columns per tensor-memory load
@@ -596,7 +623,7 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
       // elected thread stores it (out-of-range rows and columns are clipped).
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("bar.sync 1, %0;" ::"n"(Shape<PH>::dec_warps * 32) : "memory");
-      if (have && warp == 2 && lane == 0) {
+      if (have && warp == 2 && lane == 0 && !*abort_flag) {
         asm volatile(
             "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                 reinterpret_cast<uint64_t>(&tmY)),
@@ -638,12 +665,20 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
           const uint32_t remote =
               mapa_shared(smem_u32(recv + ((size_t)slot * wmax + c8) * kBM + row), (uint32_t)bb);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) st_cluster_f32(remote + 4u * kBM * j, __uint_as_float(r[j]));
+          for (int j = 0; j < 8; ++j)
+            st_cluster_f32(remote + 4u * kBM * j, __uint_as_float(r[j]) * row_pow2);
         }
       }
     }
+    // A rank whose wait ran out tells every other rank: then no rank stores
+    // (Y is left untouched after WQMM_ERR_TIMEOUT).
+    if (threadIdx.x == 0 && *abort_flag) {
+      for (int bb = 0; bb < C; ++bb)
+        if (bb != rank)
+          st_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), (uint32_t)bb), 1u);
+    }
     cluster_sync();  // every partial has arrived
-    if (warp >= 2 && have) {
+    if (warp >= 2 && have && !*abort_flag) {
       const int q = warp & 3, j4 = (warp - 2) >> 2;
       const int row = q * 32 + lane;
       const int n = n0 + row;
@@ -662,7 +697,7 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
         for (int src = 0; src < C; ++src) {
           if (src == rank) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] += __uint_as_float(r[j]);
+            for (int j = 0; j < 8; ++j) acc[j] += __uint_as_float(r[j]) * row_pow2;
           } else {
             const int slot = src < rank ? src : src - 1;
             const float* pv = recv + ((size_t)slot * wmax + c8) * kBM + row;

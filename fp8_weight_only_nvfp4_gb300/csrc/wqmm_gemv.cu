@@ -660,6 +660,12 @@ constexpr size_t kFastSmemLimit = 200 * 1024;
 // the activation slice small enough for shared memory.
 bool plan_fast(const GemvArgs& a, FastPlan& pl) {
   if (a.M < 1 || a.M > 8 || a.K % 32 != 0 || ilog2(a.bs) < 4) return false;
+  // FP8 weights with FP16 activations and blocks under 128 k would fold
+  // e4m3 * b_scale into an FP16 operand, which overflows for b_scale above
+  // about 146; the general kernel's TF32 operands have the FP32 range.
+  // (With blocks of 128 k or more the scale is applied in FP32 after the
+  // MMAs on exact E4M3 operands.)
+  if (a.kind == 1 && a.dtype == 0 && a.bs < 128) return false;
   if (a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 30)) return false;
   const DeviceInfo& d = device_info();
   const int64_t groups = (a.N + kFastRows - 1) / kFastRows;
@@ -857,17 +863,13 @@ __global__ void __launch_bounds__(kTThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) ge
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
 
-  // Epilogue constants (global scale, bias) do not depend on the previous
-  // kernel: fetched now, off the critical path at the end.
+  // Epilogue constants (global scale, bias): read by rank 0's consumers right
+  // after their first stage has landed.  That stage holds activation bytes
+  // copied after the producer's dependency wait, so these reads are ordered
+  // after the previous kernel's writes (the bias may be that kernel's output)
+  // and their latency is hidden behind the main loop.
   const int ep_row0 = row_base + (warp < kTCons ? warp : 0) * 16 + g;
   float ep_gs = 0.f, ep_b0 = 0.f, ep_b1 = 0.f;
-  if (warp < kTCons && rank == 0) {
-    ep_gs = __ldg(p.gscale);
-    if (p.bias != nullptr) {
-      if (ep_row0 < p.N) ep_b0 = act_to_f32<DT>(__ldg(p.bias + ep_row0));
-      if (ep_row0 + 8 < p.N) ep_b1 = act_to_f32<DT>(__ldg(p.bias + ep_row0 + 8));
-    }
-  }
 
   if (warp == kTCons) {
     // ---------------- producer ----------------
@@ -970,7 +972,16 @@ __global__ void __launch_bounds__(kTThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) ge
       }
       const int st_used = st;
       if (++st == NS) { st = 0; ph ^= 1u; }
-      if (i == 0) pdl_launch_dependents();
+      if (i == 0) {
+        pdl_launch_dependents();
+        if (rank == 0) {
+          ep_gs = ld_global_f32(p.gscale);
+          if (p.bias != nullptr) {
+            if (ep_row0 < p.N) ep_b0 = act_to_f32<DT>(ld_global_u16(p.bias + ep_row0));
+            if (ep_row0 + 8 < p.N) ep_b1 = act_to_f32<DT>(ld_global_u16(p.bias + ep_row0 + 8));
+          }
+        }
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t h0 = e4m3x2_to_f16x2(sb[h][0]);
@@ -1027,6 +1038,9 @@ __global__ void __launch_bounds__(kTThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) ge
         const uint32_t local = smem_u32(red + ((rank * kTCons + warp) * NT + j) * 32 + lane);
         st_cluster_f32x4(mapa_shared(local, 0), acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
       }
+      // A rank whose wait ran out tells rank 0, which then stores nothing.
+      if (rank != 0 && lane == 0 && *abort_flag)
+        st_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), 0), 1u);
     }
     cluster_sync();
     if (rank != 0 || !owner) return;
@@ -1042,6 +1056,8 @@ __global__ void __launch_bounds__(kTThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) ge
   } else if (!owner) {
     return;
   }
+  // After a wait that ran out (WQMM_ERR_TIMEOUT) Y is left untouched.
+  if (*abort_flag) return;
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll

@@ -26,7 +26,14 @@
  *  - K == 0 with a non-empty output writes Y = bias (or zeros).
  *  - No entry point traps or aborts.  Waits inside the kernels are bounded;
  *    a wait that runs out records WQMM_ERR_TIMEOUT in a device word that
- *    wqmm_device_status() reports.
+ *    wqmm_device_status() reports, and that call leaves Y untouched.
+ *  - Weights are parameters.  The NVFP4 decode GEMV starts copying B_packed
+ *    and weight_scale into shared memory before the kernel launched just
+ *    before it on `stream` has finished (programmatic dependent launch), so
+ *    those two must not be written by that immediately preceding kernel.
+ *    Every other input (A, weight_scale_2, b_scale, bias, a_scale) is read
+ *    only after all earlier work on the stream has completed; a bias may be
+ *    the previous call's output.
  *  - Thread safety: calls may be issued from several host threads at once.
  *    Per-device setup (kernel attributes, driver entry points) runs once.
  */
@@ -102,7 +109,12 @@ int fp4_weight_matmul(const void* A, const uint8_t* B_packed,
  *   Y        [M, N] (dtype).
  *   block_size must be a positive multiple of 16.
  * Paths as for fp4_weight_matmul (the GEMM needs K % 16 == 0).
- * Accuracy bound as for fp4_weight_matmul.
+ * Accuracy bound as for fp4_weight_matmul, for any finite b_scale: with FP16
+ * activations no path rounds e4m3 * b_scale into an FP16 operand, which
+ * would overflow above |b_scale| ~ 146 (the GEMM divides each weight row's
+ * block scales by a power of two and multiplies it back in FP32; the GEMV
+ * applies blocks of 128 k or more in FP32 after the MMAs and takes TF32
+ * operands for smaller blocks).
  */
 int fp8_weight_matmul(const void* A, const uint8_t* B, const float* b_scale,
                       const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
@@ -143,9 +155,10 @@ int fp8_quantize_dequantize_activation(const void* A, const float* a_scale, void
 
 /*
  * fp4_quantize_activation -- NVFP4 quantization of an activation, the first
- * step of the native FP4 x FP4 path of [FP4] §6 ("quantize activation A to
- * packed NVFP4 E2M1 with per-16-block E4M3 scales").  The page gives no
- * formula; per 16-element block of each row of A:
+ * step of the native FP4 x FP4 path of [FP4] §6: the activation takes the
+ * weight's format (two E2M1 codes per byte, one E4M3 scale per 16
+ * elements).  The page gives no formula; per 16-element block of each row
+ * of A:
  *     scale = E4M3(fp32(amax / 6))          RNE, saturating at 448
  *     code  = E2M1(fp32(a / e4m3(scale)))   RNE, ties to the even code,
  *                                           saturating at 6, sign of a kept;

@@ -292,8 +292,9 @@ uint8_t e2m1_rne_satfinite(float f) {
 }
 
 // NVFP4 activation quantization, one 16-element block of one row ([FP4] §6,
-// "Native SM120 FP4 x FP4 Path", step 1: "quantize activation A to packed
-// NVFP4 E2M1 with per-16-block E4M3 scales").  The page gives no formula;
+// the native SM120 FP4 x FP4 path, step 1, which turns the activation into
+// the weight's own format: two E2M1 codes per byte and one E4M3 scale per 16
+// elements).  The page gives no formula;
 // the reading taken (plainest, no activation global scale since the page
 // names none):
 //   amax  = max |a| over the block (a exact in float32)

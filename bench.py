@@ -517,7 +517,18 @@ def bench_also(gpu, args, peaks):
     tf = 2 * M * N * K / dt / 1e12
     out[f"fp8_prefill_M{M}_N{N}_K{K}"] = {"TFLOP/s": round(tf, 1), "frac": round(tf / tf_peak, 4),
                                           "ms": round(dt * 1e3, 3)}
-    del B8, s8, A, Y
+    # W8A8 prefill through the caller-workspace entry point: one pass that
+    # quantize-dequantizes A to FP8 into the workspace, then the same GEMM.
+    a_sc = torch.full((1,), 0.01, device=gpu.dev, dtype=torch.float32)
+    ws = torch.empty(wq.fp8_w8a8_workspace_bytes(M, K), dtype=torch.uint8, device=gpu.dev)
+    fn = lambda: wq.fp8_weight_matmul_w8a8_ws(A, a_sc, B8, s8, ws, None, 128, out=Y,
+                                              stream=gpu.stream)
+    dt_w = gpu.time_each(fn, reps=5, warmup=2)
+    tf = 2 * M * N * K / dt_w / 1e12
+    out[f"w8a8_prefill_M{M}_N{N}_K{K}"] = {"TFLOP/s": round(tf, 1), "frac": round(tf / tf_peak, 4),
+                                           "ms": round(dt_w * 1e3, 3),
+                                           "vs_weight_only": round(dt / dt_w, 3)}
+    del B8, s8, A, Y, ws, a_sc
     return out
 
 
@@ -683,6 +694,17 @@ def run_only(name, m, reps):
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
         fn = lambda: wq.fp8_weight_matmul(A, B, sc, None, 128, out=Y, stream=gpu.stream)
         work = gemv_bytes(M, N, K, 128, kind="fp8") / 1e9, "GB/s"
+    elif name == "w8a8_prefill":
+        M, N, K = (m or 8192), 17408, 5120
+        B = gpu.t(wl.gen_fp8_weight(N, K, 900))
+        sc = gpu.t(wl.gen_fp8_scale(N, wl.scale_cols(K, 128), 0.001, 0.02, 900))
+        A = torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16)
+        a_sc = torch.full((1,), 0.01, device=gpu.dev, dtype=torch.float32)
+        ws = torch.empty(wq.fp8_w8a8_workspace_bytes(M, K), dtype=torch.uint8, device=gpu.dev)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+        fn = lambda: wq.fp8_weight_matmul_w8a8_ws(A, a_sc, B, sc, ws, None, 128, out=Y,
+                                                  stream=gpu.stream)
+        work = 2 * M * N * K / 1e12, "TFLOP/s"
     elif name == "decode_step":
         print(json.dumps(decode_step(gpu, (m or 4,), reps=reps)), flush=True)
         return

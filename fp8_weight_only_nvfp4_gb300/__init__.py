@@ -15,8 +15,10 @@ Torch-tensor wrappers (same names):
   ("MatMulBlockQuantizedFp4Weight - CUDA Operator Documentation" §1).
 * ``fp8_weight_matmul(A, B, b_scale, bias=None, block_size=128, out=None)``
   ("MatMulBlockQuantizedFp8Weight - CUDA Operator Documentation" §1).
-* ``fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias=None, block_size=128, out=None)``
-  and ``fp8_quantize_dequantize_activation(A, a_scale)`` ("MatMulBlockQuantizedFp8Weight -
+* ``fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias=None, block_size=128, out=None)``,
+  ``fp8_weight_matmul_w8a8_ws(A, a_scale, B, b_scale, workspace, ...)`` (prefill-sized M
+  with a caller-owned workspace of ``fp8_w8a8_workspace_bytes(M, K)`` bytes) and
+  ``fp8_quantize_dequantize_activation(A, a_scale)`` ("MatMulBlockQuantizedFp8Weight -
   CUDA Operator Documentation" §6, the optional W8A8 activation path).
 * ``fp4_quantize_activation(A)`` and ``fp4_quantize_dequantize_activation(A)``
   ("MatMulBlockQuantizedFp4Weight - CUDA Operator Documentation" §6, step 1 of the
@@ -33,7 +35,8 @@ import threading
 
 __all__ = [
     "WqmmError", "lib", "library_path", "fp4_weight_matmul", "fp8_weight_matmul",
-    "fp8_weight_matmul_w8a8", "fp8_quantize_dequantize_activation",
+    "fp8_weight_matmul_w8a8", "fp8_weight_matmul_w8a8_ws", "fp8_w8a8_workspace_bytes",
+    "fp8_quantize_dequantize_activation",
     "fp4_quantize_activation", "fp4_quantize_dequantize_activation",
     "fp4_dequantize", "fp8_dequantize", "device_status", "FP16", "BF16",
 ]
@@ -53,6 +56,7 @@ STATUS = {
 
 # Exported C symbols, in header order.
 SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
+           "fp8_weight_matmul_w8a8_ws", "fp8_w8a8_workspace_bytes",
            "fp8_quantize_dequantize_activation", "fp4_quantize_activation",
            "fp4_quantize_dequantize_activation", "fp4_dequantize", "fp8_dequantize",
            "wqmm_status_string", "wqmm_device_status", "wqmm_selftest_wait_timeout",
@@ -85,6 +89,10 @@ def lib():
         L.fp4_weight_matmul.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P]
         L.fp8_weight_matmul.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
         L.fp8_weight_matmul_w8a8.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P]
+        L.fp8_weight_matmul_w8a8_ws.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P, I64,
+                                                P]
+        L.fp8_w8a8_workspace_bytes.argtypes = [I64, I64]
+        L.fp8_w8a8_workspace_bytes.restype = I64
         L.fp8_quantize_dequantize_activation.argtypes = [P, P, P, I64, I, P]
         L.fp4_quantize_activation.argtypes = [P, P, P, I64, I64, I, P]
         L.fp4_quantize_dequantize_activation.argtypes = [P, P, I64, I64, I, P]
@@ -96,7 +104,7 @@ def lib():
         L.wqmm_selftest_wait_timeout.argtypes = [P]
         L.wqmm_version.argtypes = []
         for name in ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
-                     "fp8_quantize_dequantize_activation", "fp4_dequantize",
+                     "fp8_weight_matmul_w8a8_ws", "fp8_quantize_dequantize_activation", "fp4_dequantize",
                      "fp8_dequantize", "wqmm_device_status", "wqmm_version"):
             getattr(L, name).restype = I
         _lib = L
@@ -258,6 +266,32 @@ def fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias=None, block_size=128, ou
                                           _ptr(bias), _ptr(out), M, N, K, int(block_size),
                                           _dt(A.dtype), _stream(stream, dev))
     _check(st, "fp8_weight_matmul_w8a8")
+    return out
+
+
+def fp8_w8a8_workspace_bytes(M, K) -> int:
+    """Workspace bytes fp8_weight_matmul_w8a8_ws needs for an [M, K] activation."""
+    return int(lib().fp8_w8a8_workspace_bytes(int(M), int(K)))
+
+
+def fp8_weight_matmul_w8a8_ws(A, a_scale, B, b_scale, workspace, bias=None, block_size=128,
+                              out=None, stream=None):
+    """FP8 page §6 W8A8 path for prefill-sized M: A_deq is written once into
+    `workspace` (a contiguous CUDA tensor of at least
+    fp8_w8a8_workspace_bytes(M, K) bytes, any dtype) and the FP8 weight-only
+    matmul runs on it; bit-identical to fp8_quantize_dequantize_activation
+    followed by fp8_weight_matmul.  Up to 8 rows this is fp8_weight_matmul_w8a8."""
+    torch = _torch()
+    dev, M, N, K, out = _fp8_common(A, B, b_scale, bias, block_size, out)
+    _check_a_scale(a_scale, dev)
+    _need(workspace, "workspace", dev)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        st = lib().fp8_weight_matmul_w8a8_ws(_ptr(A), _ptr(a_scale), _ptr(B), _ptr(b_scale),
+                                             _ptr(bias), _ptr(out), M, N, K, int(block_size),
+                                             _dt(A.dtype), _ptr(workspace), nbytes,
+                                             _stream(stream, dev))
+    _check(st, "fp8_weight_matmul_w8a8_ws")
     return out
 
 

@@ -253,6 +253,54 @@ int fp8_weight_matmul_w8a8(const void* A, const float* a_scale, const uint8_t* B
   return WQMM_OK;
 }
 
+int64_t fp8_w8a8_workspace_bytes(int64_t M, int64_t K) {
+  if (M <= 8 || K <= 0 || M >= kMaxDim || K >= kMaxDim) return 0;
+  return M * K * 2;
+}
+
+int fp8_weight_matmul_w8a8_ws(const void* A, const float* a_scale, const uint8_t* B,
+                              const float* b_scale, const void* bias, void* Y, int64_t M,
+                              int64_t N, int64_t K, int block_size, int dtype, void* workspace,
+                              int64_t workspace_bytes, void* stream) {
+  // Up to 8 rows the activation is rounded inside the decode GEMV's loads:
+  // no workspace is used.
+  if (M <= 8 || N == 0 || K == 0)
+    return fp8_weight_matmul_w8a8(A, a_scale, B, b_scale, bias, Y, M, N, K, block_size, dtype,
+                                  stream);
+  int r = check_common(M, N, K, block_size, dtype);
+  if (r != WQMM_OK) return r;
+  if (block_size % 16 != 0) return WQMM_ERR_UNSUPPORTED;
+  if (!Y || !A || !B || !b_scale || !a_scale) return WQMM_ERR_INVALID_ARG;
+  const int64_t need = fp8_w8a8_workspace_bytes(M, K);
+  if (!workspace || workspace_bytes < need) return WQMM_ERR_INVALID_ARG;
+  // The workspace receives A_deq while A is read and before Y is written:
+  // it may overlap neither.
+  const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + (uintptr_t)need;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(A), a1 = a0 + (uintptr_t)(M * K * 2);
+  const uintptr_t y0 = reinterpret_cast<uintptr_t>(Y), y1 = y0 + (uintptr_t)(M * N * 2);
+  if ((w0 < a1 && a0 < w1) || (w0 < y1 && y0 < w1)) return WQMM_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || !aligned16(Y) || !aligned16(A) || !aligned16(B) ||
+      !aligned16(b_scale) || !aligned_n(a_scale, 4) || (bias && !aligned_n(bias, 2)))
+    return WQMM_ERR_MISALIGNED;
+  if (current_device() < 0) return WQMM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  r = launch_fp8_qdq_activation(A, a_scale, workspace, M * K, dtype, st);
+  if (r != WQMM_OK) return r;
+  GemvArgs a{};
+  a.kind = 1;
+  a.A = workspace;
+  a.B = B;
+  a.fscale = b_scale;
+  a.bias = bias;
+  a.Y = Y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bs = block_size;
+  a.dtype = dtype;
+  return matmul_common(a, st);
+}
+
 int fp8_quantize_dequantize_activation(const void* A, const float* a_scale, void* out,
                                        int64_t count, int dtype, void* stream) {
   if (dtype != WQMM_FP16 && dtype != WQMM_BF16) return WQMM_ERR_INVALID_ARG;

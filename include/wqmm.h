@@ -135,13 +135,46 @@ int fp8_weight_matmul(const void* A, const uint8_t* B, const float* b_scale,
  * one RNE to dtype; exactly fp8_quantize_dequantize_activation.
  * Paths: the decode GEMV for every M (per 8-row group above 8 rows, each
  * group streaming the whole weight); for prefill-sized M the cheaper route
- * is fp8_quantize_dequantize_activation into a caller-owned [M, K] buffer
- * followed by fp8_weight_matmul, which gives the same A_deq bit for bit.
+ * is fp8_weight_matmul_w8a8_ws below (a caller-owned [M, K] workspace),
+ * which gives the same A_deq bit for bit.
  * Accuracy: the bound of fp8_weight_matmul with A_deq in place of A.
  */
 int fp8_weight_matmul_w8a8(const void* A, const float* a_scale, const uint8_t* B,
                            const float* b_scale, const void* bias, void* Y, int64_t M,
                            int64_t N, int64_t K, int block_size, int dtype, void* stream);
+
+/*
+ * fp8_weight_matmul_w8a8_ws -- the W8A8 path of fp8_weight_matmul_w8a8 for
+ * prefill-sized M, with a caller-owned workspace:
+ * [FP8] §6 Optional W8A8 Activation Path (A_deq = fp8_e4m3(A / a_scale) *
+ * a_scale, then the FP8 weight-only product on A_deq).
+ * For M <= 8 (or an empty output, or K == 0) it is fp8_weight_matmul_w8a8
+ * itself and the workspace is not used.  Above 8 rows it writes A_deq once
+ * into `workspace` ([M, K] in dtype, as fp8_quantize_dequantize_activation)
+ * and runs fp8_weight_matmul on it (the fused tcgen05 GEMM where its
+ * alignment holds), so each weight byte is read once per 256-token tile
+ * instead of once per 8 rows; the result is bit-identical to those two calls.
+ *   workspace        device pointer, 16-byte aligned, at least
+ *                    fp8_w8a8_workspace_bytes(M, K) bytes, owned by the
+ *                    caller; it may overlap neither A nor Y and is
+ *                    overwritten (contents undefined afterwards).
+ *   workspace_bytes  its size in bytes.
+ * Other arguments, layouts and errors as for fp8_weight_matmul_w8a8; a NULL
+ * or too small workspace (M > 8) or one overlapping A or Y -> INVALID_ARG;
+ * a workspace not 16-byte aligned -> MISALIGNED.  Checks run on the host
+ * before any launch; the two launches are asynchronous on `stream`.
+ */
+int fp8_weight_matmul_w8a8_ws(const void* A, const float* a_scale, const uint8_t* B,
+                              const float* b_scale, const void* bias, void* Y, int64_t M,
+                              int64_t N, int64_t K, int block_size, int dtype, void* workspace,
+                              int64_t workspace_bytes, void* stream);
+
+/*
+ * fp8_w8a8_workspace_bytes -- workspace size fp8_weight_matmul_w8a8_ws needs
+ * for an [M, K] activation: 2 * M * K bytes when M > 8, else 0 (also 0 for
+ * K <= 0 or sizes beyond the library's 2^31 limit).  Host-only, no CUDA call.
+ */
+int64_t fp8_w8a8_workspace_bytes(int64_t M, int64_t K);
 
 /*
  * fp8_quantize_dequantize_activation -- out = A_deq as defined above, for

@@ -127,3 +127,29 @@ def test_torch_wrappers_refuse_cpu_tensors(L):
     ws2 = torch.ones(1)
     with pytest.raises(ValueError):
         wq.fp4_weight_matmul(A, B, ws, ws2)
+
+
+def test_w8a8_workspace_argument_checks(L):
+    """fp8_weight_matmul_w8a8_ws: the workspace is checked on the host (size,
+    overlap with A or Y, alignment) before any CUDA call."""
+    size = L.fp8_w8a8_workspace_bytes
+    assert size(4, 32) == 0 and size(8, 32) == 0     # the fused GEMV needs none
+    assert size(9, 32) == 9 * 32 * 2
+    assert size(0, 32) == 0 and size(9, 0) == 0
+    assert size(1 << 31, 32) == 0                     # beyond the library's limit
+    A, Y, W = P(0x100000), P(0x200000), P(0x400000)
+    need = 16 * 64 * 2
+
+    def f(M=16, K=64, ws=W, nbytes=need, a=A, y=Y, **kw):
+        return L.fp8_weight_matmul_w8a8_ws(a, kw.get("asc", FAKE), FAKE, FAKE, None, y, M,
+                                           kw.get("N", 32), K, kw.get("bs", 128),
+                                           kw.get("dt", 1), ws, nbytes, None)
+    assert f(ws=None) == 1                  # M > 8 needs a workspace
+    assert f(nbytes=need - 1) == 1          # too small
+    assert f(ws=P(0x100000 + 64)) == 1      # overlaps A
+    assert f(ws=P(0x200000 - 16)) == 1      # overlaps Y
+    assert f(ws=P(0x400001)) == 3           # misaligned
+    assert f(asc=None) == 1                 # NULL a_scale
+    assert f(bs=100) == 2
+    assert f(dt=5) == 1
+    assert f(M=0, a=None, y=None, ws=None) == 0   # empty output: OK, no launch

@@ -138,3 +138,83 @@ def test_w8a8_k0_fills_bias():
     Y = wq.fp8_weight_matmul_w8a8(A, _scale_dev(1.0), B, s, act_to_dev(bias, dtype))
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bits_of(Y), np.broadcast_to(bias, (3, 24)))
+
+
+# ---------------------------------------------------------------------------
+# Prefill-sized M with a caller-owned workspace (fp8_weight_matmul_w8a8_ws)
+# ---------------------------------------------------------------------------
+
+def _ws_gpu(d, a_scale, M, K, block_size, extra=0):
+    ws = torch.empty(wq.fp8_w8a8_workspace_bytes(M, K) + extra, dtype=torch.uint8, device=DEV)
+    Y = wq.fp8_weight_matmul_w8a8_ws(d["A"], _scale_dev(a_scale), d["B"], d["s"], ws, d["bias"],
+                                     block_size=block_size)
+    torch.cuda.synchronize()
+    assert wq.device_status() == 0
+    return Y, ws
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("M,N,K,bs", [(9, 384, 512, 128), (64, 256, 1024, 128),
+                                      (300, 384, 640, 64), (40, 17, 1000, 128)])
+def test_w8a8_ws_against_oracle(M, N, K, bs, dtype):
+    """Above 8 rows A_deq goes through the workspace into the FP8 GEMM (or the
+    general GEMV for odd shapes); the product is held to the matmul bound
+    against the oracle's FP8 matmul of the oracle's A_deq."""
+    a_scale = 0.0213
+    p = wl.make_fp8(M, N, K, bs, dtype, seed=M + N + K, bias_sigma=0.1)
+    Y, _ = _ws_gpu(fp8_dev(p), a_scale, M, K, bs)
+    assert_within_tolerance(Y, *_w8a8_ref(p, a_scale), dtype, f"w8a8 ws {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [9, 256, 1000])
+def test_w8a8_ws_equals_two_call_route(M):
+    """The workspace path is quantize-dequantize followed by fp8_weight_matmul:
+    bit-identical to those two calls, and the workspace holds A_deq."""
+    p = wl.make_fp8(M, 512, 1024, 128, oracle.BF16, seed=M, bias_sigma=0.1)
+    a_scale = 0.05
+    d = fp8_dev(p)
+    Y1, ws = _ws_gpu(d, a_scale, M, 1024, 128)
+    Aq = wq.fp8_quantize_dequantize_activation(d["A"], _scale_dev(a_scale))
+    Y2 = wq.fp8_weight_matmul(Aq, d["B"], d["s"], d["bias"], block_size=128)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    assert torch.equal(ws.view(torch.int16).view(M, 1024), Aq.view(torch.int16))
+
+
+def test_w8a8_ws_small_m_is_the_fused_gemv():
+    """Up to 8 rows the workspace is not used: same output as
+    fp8_weight_matmul_w8a8, bit for bit, and the workspace untouched."""
+    p = wl.make_fp8(6, 256, 2048, 128, oracle.BF16, seed=7, bias_sigma=0.1)
+    d = fp8_dev(p)
+    Y1 = wq.fp8_weight_matmul_w8a8(d["A"], _scale_dev(0.05), d["B"], d["s"], d["bias"],
+                                   block_size=128)
+    ws = torch.full((64,), 0x5A, dtype=torch.uint8, device=DEV)
+    Y2 = wq.fp8_weight_matmul_w8a8_ws(d["A"], _scale_dev(0.05), d["B"], d["s"], ws, d["bias"],
+                                      block_size=128)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    assert bool((ws == 0x5A).all())
+
+
+def test_w8a8_ws_prefill_sampled():
+    """The FP8 prefill shape (M = 8192, N = 17408, K = 5120, bs = 128) through the
+    workspace path: bit-identical to the two-call route, and 4096 sampled
+    outputs within the bound of the oracle's FP8 matmul of the oracle's A_deq."""
+    p = wl.fp8_problem(8192, N=17408, K=5120, bias_sigma=0.02)
+    a_scale = 0.01
+    d = fp8_dev(p)
+    Y, _ = _ws_gpu(d, a_scale, p.M, p.K, p.block_size)
+    Aq = wq.fp8_quantize_dequantize_activation(d["A"], _scale_dev(a_scale))
+    Y2 = wq.fp8_weight_matmul(Aq, d["B"], d["s"], d["bias"], block_size=p.block_size)
+    torch.cuda.synchronize()
+    assert wq.device_status() == 0
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    rng = np.random.default_rng(17)
+    ms = rng.integers(0, p.M, 4096)
+    ns = rng.integers(0, p.N, 4096)
+    Aq_h = oracle.fp8_qdq_activation(p.A[ms], a_scale, p.dtype)
+    yref, sabs = oracle.fp8_matmul_sampled(Aq_h, p.B, p.b_scale, p.bias, p.K, p.block_size,
+                                           p.dtype, np.arange(4096), ns)
+    got = bits_of(Y).reshape(p.M, p.N)[ms, ns]
+    Yg = torch.from_numpy(got.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+    assert_within_tolerance(Yg, yref, sabs, p.dtype, "w8a8 ws prefill sampled")

@@ -36,6 +36,7 @@ import threading
 __all__ = [
     "WqmmError", "lib", "library_path", "fp4_weight_matmul", "fp8_weight_matmul",
     "fp8_weight_matmul_w8a8", "fp8_weight_matmul_w8a8_ws", "fp8_w8a8_workspace_bytes",
+    "fp8_weight_matmul_w8a8_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fp8_quantize_dequantize_activation",
     "fp4_quantize_activation", "fp4_quantize_dequantize_activation",
     "fp4_dequantize", "fp8_dequantize", "device_status", "FP16", "BF16",
@@ -43,6 +44,10 @@ __all__ = [
 
 FP16 = 0
 BF16 = 1
+
+# WQMM_NOALLOC_SCRATCH_BYTES of include/wqmm.h: fp8_weight_matmul_w8a8_noalloc
+# takes problems with 2 * M * K up to this many bytes.
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libwqmm.so")
@@ -57,7 +62,7 @@ STATUS = {
 # Exported C symbols, in header order.
 SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
            "fp8_weight_matmul_w8a8_ws", "fp8_w8a8_workspace_bytes",
-           "fp8_quantize_dequantize_activation", "fp4_quantize_activation",
+           "fp8_weight_matmul_w8a8_noalloc", "fp8_quantize_dequantize_activation", "fp4_quantize_activation",
            "fp4_quantize_dequantize_activation", "fp4_dequantize", "fp8_dequantize",
            "wqmm_status_string", "wqmm_device_status", "wqmm_selftest_wait_timeout",
            "wqmm_version")
@@ -93,6 +98,7 @@ def lib():
                                                 P]
         L.fp8_w8a8_workspace_bytes.argtypes = [I64, I64]
         L.fp8_w8a8_workspace_bytes.restype = I64
+        L.fp8_weight_matmul_w8a8_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P]
         L.fp8_quantize_dequantize_activation.argtypes = [P, P, P, I64, I, P]
         L.fp4_quantize_activation.argtypes = [P, P, P, I64, I64, I, P]
         L.fp4_quantize_dequantize_activation.argtypes = [P, P, I64, I64, I, P]
@@ -104,7 +110,8 @@ def lib():
         L.wqmm_selftest_wait_timeout.argtypes = [P]
         L.wqmm_version.argtypes = []
         for name in ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
-                     "fp8_weight_matmul_w8a8_ws", "fp8_quantize_dequantize_activation", "fp4_dequantize",
+                     "fp8_weight_matmul_w8a8_ws", "fp8_weight_matmul_w8a8_noalloc",
+                     "fp8_quantize_dequantize_activation", "fp4_dequantize",
                      "fp8_dequantize", "wqmm_device_status", "wqmm_version"):
             getattr(L, name).restype = I
         _lib = L
@@ -292,6 +299,28 @@ def fp8_weight_matmul_w8a8_ws(A, a_scale, B, b_scale, workspace, bias=None, bloc
                                              _dt(A.dtype), _ptr(workspace), nbytes,
                                              _stream(stream, dev))
     _check(st, "fp8_weight_matmul_w8a8_ws")
+    return out
+
+
+def fp8_weight_matmul_w8a8_noalloc(A, a_scale, B, b_scale, out, bias=None, block_size=128,
+                                   stream=None):
+    """fp8_weight_matmul_w8a8_ws with the workspace taken from a fixed 16 MiB
+    array inside the library, for callers that may not allocate device memory
+    (2 * M * K <= NOALLOC_SCRATCH_BYTES when M > 8).  `out` is required, so
+    nothing is allocated here either.  Calls that may overlap in time on one
+    device share the array and race; the first call on a device should come
+    before any stream capture."""
+    torch = _torch()
+    if out is None:
+        raise ValueError("out is required: this entry point allocates nothing")
+    dev, M, N, K, out = _fp8_common(A, B, b_scale, bias, block_size, out)
+    _check_a_scale(a_scale, dev)
+    with torch.cuda.device(dev):
+        st = lib().fp8_weight_matmul_w8a8_noalloc(_ptr(A), _ptr(a_scale), _ptr(B), _ptr(b_scale),
+                                                  _ptr(bias), _ptr(out), M, N, K,
+                                                  int(block_size), _dt(A.dtype),
+                                                  _stream(stream, dev))
+    _check(st, "fp8_weight_matmul_w8a8_noalloc")
     return out
 
 

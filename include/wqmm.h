@@ -14,7 +14,9 @@
  * ---------------------------------------
  *  - Every tensor pointer is a DEVICE pointer (global memory of the current
  *    device), row-major and contiguous.  The caller owns every buffer.  The
- *    library allocates no device memory and keeps no per-call state.
+ *    library allocates no device memory and keeps no per-call state (its
+ *    only device data are an error word and the fixed scratch array of
+ *    fp8_weight_matmul_w8a8_noalloc, both reserved when its code loads).
  *  - `dtype` selects the activation type used for A, bias, Y and dequantized
  *    outputs: WQMM_FP16 (IEEE binary16) or WQMM_BF16 (bfloat16).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
@@ -175,6 +177,45 @@ int fp8_weight_matmul_w8a8_ws(const void* A, const float* a_scale, const uint8_t
  * K <= 0 or sizes beyond the library's 2^31 limit).  Host-only, no CUDA call.
  */
 int64_t fp8_w8a8_workspace_bytes(int64_t M, int64_t K);
+
+/* Size of the scratch array that fp8_weight_matmul_w8a8_noalloc draws on. */
+#define WQMM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * fp8_weight_matmul_w8a8_noalloc -- fp8_weight_matmul_w8a8_ws for callers
+ * that may not allocate device memory.  The source pages have no counterpart
+ * to this entry point; it computes exactly what fp8_weight_matmul_w8a8_ws
+ * computes ([FP8] §6 Optional W8A8 Activation Path), bit for bit.
+ *
+ * Who needs it: code that runs where a device allocation is not allowed or
+ * not affordable -- inference hosts that hand out all device memory through
+ * their own pool and forbid any other allocation, serving loops that must not
+ * call cudaMalloc after start-up because it can stall the device and every
+ * other stream on it, plugins whose host process owns the memory budget.
+ * Such a caller cannot provide (or cannot allocate) the [M, K] workspace of
+ * fp8_weight_matmul_w8a8_ws.  This call allocates nothing: the workspace is a
+ * fixed array of WQMM_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library,
+ * which the CUDA runtime reserves on every GPU where the library's code is
+ * loaded and which stays reserved until the process exits.
+ *
+ * Arguments, layouts and errors as for fp8_weight_matmul_w8a8_ws without
+ * `workspace` / `workspace_bytes`.  Limit: 2 * M * K <= 16 MiB for M > 8
+ * (e.g. M <= 1638 at K = 5120); a larger problem -> WQMM_ERR_UNSUPPORTED,
+ * detected on the host before any CUDA call.  M <= 8 (or an empty output,
+ * or K == 0) uses no scratch and has no such limit.
+ *
+ * Set-up: the first call on a device with M > 8 looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; a failure there
+ * -> WQMM_ERR_CUDA.  Make that first call before any stream capture begins.
+ * Nothing in the array needs to start at zero: each call writes the values
+ * it reads.  Concurrency: one array per device is shared by all calls, so
+ * calls that may overlap in time on the same device (unordered streams, or
+ * several host threads) race on it and give undefined results; order them
+ * on one stream or with events.
+ */
+int fp8_weight_matmul_w8a8_noalloc(const void* A, const float* a_scale, const uint8_t* B,
+                                   const float* b_scale, const void* bias, void* Y, int64_t M,
+                                   int64_t N, int64_t K, int block_size, int dtype, void* stream);
 
 /*
  * fp8_quantize_dequantize_activation -- out = A_deq as defined above, for

@@ -153,3 +153,27 @@ def test_w8a8_workspace_argument_checks(L):
     assert f(bs=100) == 2
     assert f(dt=5) == 1
     assert f(M=0, a=None, y=None, ws=None) == 0   # empty output: OK, no launch
+
+
+def test_noalloc_host_checks(L):
+    """fp8_weight_matmul_w8a8_noalloc: its scratch limit and argument errors
+    are reported on the host, before any CUDA call."""
+    text = open(os.path.join(ROOT, "include", "wqmm.h")).read()
+    m = re.search(r"#define WQMM_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == wq.NOALLOC_SCRATCH_BYTES
+
+    def f(M=16, N=32, K=64, bs=128, dt=1, A=FAKE, Y=P(0x200000), asc=FAKE):
+        return L.fp8_weight_matmul_w8a8_noalloc(A, asc, FAKE, FAKE, None, Y, M, N, K, bs, dt,
+                                                None)
+    lim = wq.NOALLOC_SCRATCH_BYTES
+    assert f(M=lim // (2 * 4096) + 1, K=4096) == 2      # 2*M*K just above the limit
+    assert f(M=1 << 20, K=1 << 20) == 2
+    assert f(M=1 << 31, K=64) == 2                      # beyond the library's limit
+    assert f(dt=7) == 1
+    assert f(M=-1) == 1
+    assert f(bs=0) == 1
+    assert f(bs=100) == 2
+    assert f(A=None) == 1
+    assert f(asc=None) == 1
+    assert f(Y=FAKE_ODD) == 3
+    assert f(M=0, A=None, Y=None) == 0                   # empty output: no launch

@@ -705,6 +705,15 @@ def run_only(name, m, reps):
         fn = lambda: wq.fp8_weight_matmul_w8a8_ws(A, a_sc, B, sc, ws, None, 128, out=Y,
                                                   stream=gpu.stream)
         work = 2 * M * N * K / 1e12, "TFLOP/s"
+    elif name == "f4f4_prefill":
+        M, N, K = (m or 8192), 17408, 5120
+        ly = gpu.fp4_layers(M, N, K, 1, seed0=700, bias=True)[0]
+        A = torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16)
+        qc, qs = wq.fp4_quantize_activation(A)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+        fn = lambda: wq.fp4_fp4_matmul(qc, qs, ly["B"], ly["ws"], ly["ws2"], ly["bias"], out=Y,
+                                       stream=gpu.stream)
+        work = 2 * M * N * K / 1e12, "TFLOP/s"
     elif name == "decode_step":
         print(json.dumps(decode_step(gpu, (m or 4,), reps=reps)), flush=True)
         return

@@ -38,7 +38,7 @@ __all__ = [
     "fp8_weight_matmul_w8a8", "fp8_weight_matmul_w8a8_ws", "fp8_w8a8_workspace_bytes",
     "fp8_weight_matmul_w8a8_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fp8_quantize_dequantize_activation",
-    "fp4_quantize_activation", "fp4_quantize_dequantize_activation",
+    "fp4_quantize_activation", "fp4_quantize_dequantize_activation", "fp4_fp4_matmul",
     "fp4_dequantize", "fp8_dequantize", "device_status", "FP16", "BF16",
 ]
 
@@ -63,7 +63,8 @@ STATUS = {
 SYMBOLS = ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
            "fp8_weight_matmul_w8a8_ws", "fp8_w8a8_workspace_bytes",
            "fp8_weight_matmul_w8a8_noalloc", "fp8_quantize_dequantize_activation", "fp4_quantize_activation",
-           "fp4_quantize_dequantize_activation", "fp4_dequantize", "fp8_dequantize",
+           "fp4_quantize_dequantize_activation", "fp4_fp4_matmul", "fp4_dequantize",
+           "fp8_dequantize",
            "wqmm_status_string", "wqmm_device_status", "wqmm_selftest_wait_timeout",
            "wqmm_version")
 
@@ -102,6 +103,7 @@ def lib():
         L.fp8_quantize_dequantize_activation.argtypes = [P, P, P, I64, I, P]
         L.fp4_quantize_activation.argtypes = [P, P, P, I64, I64, I, P]
         L.fp4_quantize_dequantize_activation.argtypes = [P, P, I64, I64, I, P]
+        L.fp4_fp4_matmul.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I, P]
         L.fp4_dequantize.argtypes = [P, P, P, P, I64, I64, I, I, P]
         L.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, I, P]
         L.wqmm_status_string.argtypes = [I]
@@ -111,7 +113,7 @@ def lib():
         L.wqmm_version.argtypes = []
         for name in ("fp4_weight_matmul", "fp8_weight_matmul", "fp8_weight_matmul_w8a8",
                      "fp8_weight_matmul_w8a8_ws", "fp8_weight_matmul_w8a8_noalloc",
-                     "fp8_quantize_dequantize_activation", "fp4_dequantize",
+                     "fp8_quantize_dequantize_activation", "fp4_fp4_matmul", "fp4_dequantize",
                      "fp8_dequantize", "wqmm_device_status", "wqmm_version"):
             getattr(L, name).restype = I
         _lib = L
@@ -385,6 +387,41 @@ def fp4_quantize_dequantize_activation(A, out=None, stream=None):
         st = lib().fp4_quantize_dequantize_activation(_ptr(A), _ptr(out), M, K, _dt(A.dtype),
                                                       _stream(stream, dev))
     _check(st, "fp4_quantize_dequantize_activation")
+    return out
+
+
+def fp4_fp4_matmul(A_packed, A_scale, B_packed, weight_scale, weight_scale_2, bias=None,
+                   out=None, dtype=None, stream=None):
+    """FP4 x FP4 product on the block-scaled tensor core (FP4 page §6, steps
+    2-3): A_packed / A_scale as returned by fp4_quantize_activation, the
+    NVFP4 weight with 16-element blocks.  The output type is out.dtype, else
+    bias.dtype, else `dtype` (default bfloat16).  K must be a multiple of 256."""
+    torch = _torch()
+    dev = _device_of(A_packed)
+    if B_packed.dim() != 2:
+        raise ValueError(f"B_packed must be 2-D [N, K/2], got shape {tuple(B_packed.shape)}")
+    N, K = B_packed.shape[0], 2 * B_packed.shape[1]
+    if A_packed.dim() < 1 or A_packed.shape[-1] * 2 != K:
+        raise ValueError(f"A_packed.shape[-1] * 2 != K={K}")
+    lead = tuple(A_packed.shape[:-1])
+    M = A_packed.numel() // (K // 2) if K else int(torch.tensor(lead).prod())
+    S = _scale_cols(K, 16)
+    _need(A_packed, "A_packed", dev, (torch.uint8,))
+    _need(A_scale, "A_scale", dev, _byte_dtypes(), shape=lead + (S,))
+    _need(B_packed, "B_packed", dev, (torch.uint8,))
+    _need(weight_scale, "weight_scale", dev, _byte_dtypes(), shape=(N, S))
+    _need(weight_scale_2, "weight_scale_2", dev, (torch.float32,), numel=1)
+    ydt = out.dtype if out is not None else (bias.dtype if bias is not None
+                                             else (dtype or torch.bfloat16))
+    _need(bias, "bias", dev, (ydt,), numel=N)
+    if out is None:
+        out = torch.empty(*lead, N, dtype=ydt, device=dev)
+    _need(out, "out", dev, _act_dtypes(), shape=lead + (N,))
+    with torch.cuda.device(dev):
+        st = lib().fp4_fp4_matmul(_ptr(A_packed), _ptr(A_scale), _ptr(B_packed),
+                                  _ptr(weight_scale), _ptr(weight_scale_2), _ptr(bias), _ptr(out),
+                                  M, N, K, _dt(ydt), _stream(stream, dev))
+    _check(st, "fp4_fp4_matmul")
     return out
 
 

@@ -338,6 +338,42 @@ int fp4_quantize_dequantize_activation(const void* A, void* out, int64_t M, int6
   return launch_nvfp4_qdq_activation(A, out, M, K, dtype, static_cast<cudaStream_t>(stream));
 }
 
+int fp4_fp4_matmul(const uint8_t* A_packed, const uint8_t* A_scale, const uint8_t* B_packed,
+                   const uint8_t* weight_scale, const float* weight_scale_2, const void* bias,
+                   void* Y, int64_t M, int64_t N, int64_t K, int dtype, void* stream) {
+  int r = check_common(M, N, K, 16, dtype);
+  if (r != WQMM_OK) return r;
+  if (K % 2 != 0) return WQMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WQMM_OK;
+  if (!Y) return WQMM_ERR_INVALID_ARG;
+  if (K > 0 && (!A_packed || !A_scale || !B_packed || !weight_scale || !weight_scale_2))
+    return WQMM_ERR_INVALID_ARG;
+  // Stages of 256 k, and scale rows (K / 16 bytes) that the tensor copies can
+  // address: K a multiple of 256.
+  if (K % 256 != 0) return WQMM_ERR_UNSUPPORTED;
+  if (!aligned16(Y) || (K > 0 && (!aligned16(A_packed) || !aligned16(A_scale) ||
+                                  !aligned16(B_packed) || !aligned16(weight_scale) ||
+                                  !aligned_n(weight_scale_2, 4))) ||
+      (bias && !aligned_n(bias, 2)))
+    return WQMM_ERR_MISALIGNED;
+  if (current_device() < 0) return WQMM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_fill_bias(bias, Y, M, N, dtype, st);
+  F4F4Args a{};
+  a.A = A_packed;
+  a.A_scale = A_scale;
+  a.B = B_packed;
+  a.ws = weight_scale;
+  a.gscale = weight_scale_2;
+  a.bias = bias;
+  a.Y = Y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.dtype = dtype;
+  return launch_gemm_f4f4(a, st);
+}
+
 int fp4_dequantize(const uint8_t* B_packed, const uint8_t* weight_scale,
                    const float* weight_scale_2, void* out, int64_t N, int64_t K, int block_size,
                    int dtype, void* stream) {

@@ -1,0 +1,357 @@
+// wqmm_gemm_f4f4.cu -- NVFP4 x NVFP4 block-scaled tensor-core GEMM.
+//
+//   Y[m, n] = weight_scale_2 * sum_k e2m1(Aq[m, k]) e4m3(As[m, k / 16])
+//                                  * e2m1(B[n, k])  e4m3(ws[n, k / 16])   (+ bias[n])
+//
+// Steps 2 and 3 of the native FP4 x FP4 path of "MatMulBlockQuantizedFp4Weight
+// - CUDA Operator Documentation" §6 (step 1, quantizing the activation to
+// NVFP4, is wqmm_actq.cu): both operands stay packed E2M1 from global memory
+// to the tensor core, and the block-scaled MMA of the sm_100 family
+// (tcgen05.mma.kind::mxf4nvf4, 16-element blocks, unsigned E4M3 scales)
+// applies both operands' block scales itself; products are exact and
+// accumulate in FP32.  The page runs a CUTLASS kernel on SM120 and prepacks
+// the weight scales into that kernel's layout; here the scales keep the plain
+// [rows, K/16] layout of the weight format and are rearranged on chip.
+//
+// Tile: 128 weight rows (MMA M) x 256 tokens (MMA N) per CTA; K in stages of
+// 256 (one 128-byte swizzled row of packed codes per operand row), four MMAs
+// of K = 64 per stage.
+// Roles (10 warps):
+//   warp 0     TMA producer: per stage the packed weight tile [128 x 128 B] and
+//              activation tile [256 x 128 B] (K-major, 128-byte swizzle) and
+//              their scale tiles [128 x 16 B] and [256 x 16 B];
+//   warp 1     TMEM owner and MMA issuer (one elected thread);
+//   warps 2-9  scale writers, then the epilogue: warp w serves TMEM lane
+//              quarter w % 4 and takes every other stage; it moves the
+//              stage's scale bytes from shared memory to tensor memory in the
+//              layout the block-scaled MMA reads (below) with tcgen05.st.
+//              After the main loop: TMEM -> registers, * weight_scale_2,
+//              + bias, one RNE, Y through a shared-memory transpose and one
+//              tensor store (direct stores when the row pitch of Y is not a
+//              16-byte multiple).
+//
+// Scale factors in tensor memory (scale_vec::4X): one 32-bit cell per operand
+// row and 64-k chunk, byte i holding the scale of the chunk's i-th 16-element
+// block.  The cells of operand row r sit in lane r % 32 and column r / 32 of
+// the chunk's column group (4 columns for the 128 weight rows, 8 for the 256
+// tokens: rows 128..255 in the upper 4), and every lane quarter holds the same
+// copy.
+//
+// Every mbarrier wait is bounded; a wait that runs out raises a CTA-wide
+// abort flag, records WQMM_ERR_TIMEOUT and all roles drain to the TMEM
+// release at the end.
+#include <cstring>
+#include <mutex>
+
+#include "wqmm_tcgen05.cuh"
+
+namespace wqmm {
+
+namespace {
+
+constexpr int kBM = 128;              // weight rows per tile (MMA M)
+constexpr int kBN = 256;              // tokens per tile (MMA N)
+constexpr int kBK = 256;              // k per stage
+constexpr int kRowBytes = kBK / 2;    // packed bytes per operand row per stage
+constexpr int kScBytes = kBK / 16;    // scale bytes per operand row per stage
+constexpr int kStages = 4;
+constexpr int kPh = 2;                // scale-writer warps per TMEM lane quarter
+constexpr int kWriters = 4 * kPh;
+constexpr int kThreads = (2 + kWriters) * 32;
+constexpr int kTmemCols = 512;
+
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr int kActTile = kBN * kRowBytes;   // 32 KB
+constexpr int kWTile = kBM * kRowBytes;     // 16 KB
+constexpr int kActSc = kBN * kScBytes;      // 4 KB
+constexpr int kWSc = kBM * kScBytes;        // 2 KB
+constexpr int kOffAct = 0;
+constexpr int kOffW = kOffAct + kStages * kActTile;
+constexpr int kOffActSc = kOffW + kStages * kWTile;
+constexpr int kOffWSc = kOffActSc + kStages * kActSc;
+constexpr int kOffFull = kOffWSc + kStages * kWSc;
+constexpr int kOffEmpty = kOffFull + 8 * kStages;
+constexpr int kOffReady = kOffEmpty + 8 * kStages;
+constexpr int kOffAcc = kOffReady + 8 * kStages;
+constexpr int kOffSlot = kOffAcc + 8;
+constexpr int kOffAbort = kOffSlot + 4;
+constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
+constexpr uint32_t kStageBytes = kActTile + kWTile + kActSc + kWSc;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kBN * kBM * 2 <= kStages * kActTile, "Y staging fits in the activation ring");
+static_assert(kStages % kPh == 0, "a writer's parity wait follows its own previous wait");
+
+// Tensor memory: accumulator [0, 256); per stage the token scales (8 columns
+// per 64-k chunk, 32 per stage) and the weight scales (4 per chunk, 16 per
+// stage).
+constexpr int kColAcc = 0;
+constexpr int kColSfb = kBN;
+constexpr int kColSfa = kColSfb + kStages * 32;
+static_assert(kColSfa + kStages * 16 <= kTmemCols, "TMEM columns");
+
+// Instruction descriptor, kind::mxf4nvf4: A (weight) and B (tokens) E2M1
+// (format code 1), both K-major, unsigned-E4M3 scale factors (scale type 0),
+// scale-factor ids 0, N = 256, M = 128, D = FP32.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                            ((uint32_t)(kBM >> 4) << 24);
+
+// One stage: four block-scaled MMAs of K = 64, A and B stepping 32 bytes (2
+// descriptor units) along their swizzled rows, the weight scales 4 columns and
+// the token scales 8 columns per MMA; the first MMA accumulates only if
+// `accumulate`.
+__device__ __forceinline__ void mma_f4_stage(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p, t; .reg .b64 a1, a2, a3, b1, b2, b3; .reg .b32 sa1, sa2, sa3, sb1, sb2, sb3;\n\t"
+      "setp.ne.b32 p, %5, 0; setp.eq.b32 t, %5, %5;\n\t"
+      "add.u64 a1, %1, 2; add.u64 a2, %1, 4; add.u64 a3, %1, 6;\n\t"
+      "add.u64 b1, %2, 2; add.u64 b2, %2, 4; add.u64 b3, %2, 6;\n\t"
+      "add.u32 sa1, %3, 4; add.u32 sa2, %3, 8; add.u32 sa3, %3, 12;\n\t"
+      "add.u32 sb1, %4, 8; add.u32 sb2, %4, 16; add.u32 sb3, %4, 24;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %6, [%3], [%4], p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %6, [sa1], [sb1], t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a2, b2, %6, [sa2], [sb2], t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a3, b3, %6, [sa3], [sb3], t; }"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(sfa), "r"(sfb), "r"(accumulate), "r"(kIdesc)
+      : "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_f4f4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmAS, const __grid_constant__ CUtensorMap tmWS,
+                     const __grid_constant__ CUtensorMap tmY, int y_tma,
+                     const float* __restrict__ gscale, const uint16_t* __restrict__ bias,
+                     uint16_t* __restrict__ Y, int M, int N, int K, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kOffEmpty);
+  uint64_t* ready = reinterpret_cast<uint64_t*>(smem + kOffReady);
+  uint64_t* accfull = reinterpret_cast<uint64_t*>(smem + kOffAcc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBM;
+  const int m0 = blockIdx.y * kBN;
+  const int num_k = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&ready[s], 4);  // one writer warp per lane quarter
+    }
+    mbar_init(accfull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmAS);
+    prefetch_tmap(&tmWS);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool have = false;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int it = 0; it < num_k; ++it) {
+        const int s = it % kStages;
+        if (it >= kStages && !wait_bar(&empty[s], ((it / kStages) + 1) & 1, err, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        tma_load_2d(smem + kOffAct + s * kActTile, &tmA, it * kRowBytes, m0, &full[s]);
+        tma_load_2d(smem + kOffW + s * kWTile, &tmW, it * kRowBytes, n0, &full[s]);
+        tma_load_2d(smem + kOffActSc + s * kActSc, &tmAS, it * kScBytes, m0, &full[s]);
+        tma_load_2d(smem + kOffWSc + s * kWSc, &tmWS, it * kScBytes, n0, &full[s]);
+        ++issued;
+      }
+      // No copy may still be landing in shared memory when the CTA exits.
+      for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it)
+        drain_wait(&full[it % kStages], (it / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      int committed = -1;
+      const uint64_t adesc0 = desc_kmajor_sw128(smem_u32(smem + kOffW));
+      const uint64_t bdesc0 = desc_kmajor_sw128(smem_u32(smem + kOffAct));
+      for (int it = 0; it < num_k; ++it) {
+        const int s = it % kStages;
+        // ready[s] implies full[s]: each writer warp arrives only after its
+        // own wait on full[s], which covers all four copies of the stage.
+        if (!wait_bar(&ready[s], (it / kStages) & 1, err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_f4_stage(tmem + kColAcc, adesc0 + (uint64_t)((s * kWTile) >> 4),
+                     bdesc0 + (uint64_t)((s * kActTile) >> 4), tmem + kColSfa + 16 * s,
+                     tmem + kColSfb + 32 * s, it > 0 ? 1u : 0u);
+        mma_commit(&empty[s]);
+        committed = it;
+      }
+      if (ok) {
+        mma_commit(accfull);
+      } else if (committed >= 0) {
+        // MMAs still reading tensor memory must finish before the release.
+        drain_wait(&empty[committed % kStages], (committed / kStages) & 1);
+      }
+    }
+  } else {
+    // ---------------- scale writers, then the epilogue ----------------
+    const int q = warp & 3;               // TMEM lane quarter
+    const int ph = (warp - 2) >> 2;       // stage phase of this warp
+    const int row = q * 32 + lane;        // weight row within the tile
+    const int n = n0 + row;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    bool ok = true;
+    for (int it = ph; it < num_k; it += kPh) {
+      const int s = it % kStages;
+      if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      // Register j of the weight-scale store goes to column j: chunk j / 4,
+      // row group j % 4 (rows 32 (j % 4) + lane); the token-scale store has 8
+      // columns per chunk, row group (j % 8) of 32 tokens.
+      const uint8_t* wsc = smem + kOffWSc + s * kWSc;
+      const uint8_t* asc = smem + kOffActSc + s * kActSc;
+      uint32_t va[16], vb[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 r = *reinterpret_cast<const uint4*>(wsc + (32 * c + lane) * kScBytes);
+        va[c] = r.x;
+        va[4 + c] = r.y;
+        va[8 + c] = r.z;
+        va[12 + c] = r.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 r = *reinterpret_cast<const uint4*>(asc + (32 * c + lane) * kScBytes);
+        vb[c] = r.x;
+        vb[8 + c] = r.y;
+        vb[16 + c] = r.z;
+        vb[24 + c] = r.w;
+      }
+      tmem_st16(lane_base + kColSfa + 16 * s, va);
+      tmem_st32(lane_base + kColSfb + 32 * s, vb);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[s]);
+    }
+    // Epilogue: this warp's lane quarter, token-column chunks of 32 taken in
+    // turn by the quarter's kPh warps.
+    have = ok && wait_bar(accfull, 0, err, abort_flag) && !*abort_flag;
+    if (have) {
+      tc_fence_after();
+      const float gs = __ldg(gscale);
+      const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
+      uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + kOffAct);
+#pragma unroll 1
+      for (int c0 = 32 * ph; c0 < kBN; c0 += 32 * kPh) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + kColAcc + c0, r);
+        if (y_tma) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            stage_y[(c0 + j) * kBM + row] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
+        } else if (n < N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < M) Y[(int64_t)m * N + n] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
+          }
+        }
+      }
+    }
+    if (y_tma) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kWriters * 32) : "memory");
+      if (have && warp == 2 && lane == 0 && !*abort_flag) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                reinterpret_cast<uint64_t>(&tmY)),
+            "r"(n0), "r"(m0), "r"(smem_u32(smem + kOffAct))
+            : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      }
+    }
+  }
+
+  // Teardown: every tcgen05 access of this CTA is complete before the release.
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int DT>
+int launch_t(const F4F4Args& a, cudaStream_t st) {
+  const uint64_t rowb = (uint64_t)a.K / 2, scb = (uint64_t)a.K / 16;
+  CUtensorMap tmA, tmW, tmAS, tmWS, tmY;
+  if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, rowb, (uint64_t)a.M, rowb,
+                      kRowBytes, kBN, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, rowb, (uint64_t)a.N, rowb,
+                      kRowBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_tmap_2d(&tmAS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A_scale, scb, (uint64_t)a.M, scb,
+                      kScBytes, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+      !encode_tmap_2d(&tmWS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ws, scb, (uint64_t)a.N, scb,
+                      kScBytes, kBM, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+    return kCuda;
+  const CUtensorMapDataType ydt =
+      DT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  int y_tma = 0;
+  std::memset(&tmY, 0, sizeof(tmY));
+  if (a.N % 8 == 0)
+    y_tma = encode_tmap_2d(&tmY, ydt, a.Y, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.N * 2, kBM,
+                           kBN, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
+                ? 1
+                : 0;
+  static std::once_flag once[64];
+  const int dev = device_info().device;
+  if (dev < 0 || dev >= 64) return kCuda;
+  std::call_once(once[dev], [] {
+    cudaFuncSetAttribute(gemm_f4f4_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSmemBytes);
+  });
+  const dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)((a.M + kBN - 1) / kBN), 1);
+  gemm_f4f4_kernel<DT><<<grid, kThreads, kSmemBytes, st>>>(
+      tmA, tmW, tmAS, tmWS, tmY, y_tma, a.gscale, reinterpret_cast<const uint16_t*>(a.bias),
+      reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, device_error_word());
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
+}  // namespace
+
+bool gemm_f4f4_supports(const F4F4Args& a) {
+  const DeviceInfo& d = device_info();
+  if (d.cc_major != 10 || d.max_smem_optin < kSmemBytes) return false;
+  if (a.K % kBK != 0) return false;
+  return (a.M + kBN - 1) / kBN <= 65535 && a.N < (int64_t(1) << 31);
+}
+
+int launch_gemm_f4f4(const F4F4Args& a, cudaStream_t st) {
+  if (!gemm_f4f4_supports(a)) return kUnsupported;
+  return a.dtype == 1 ? launch_t<1>(a, st) : launch_t<0>(a, st);
+}
+
+}  // namespace wqmm

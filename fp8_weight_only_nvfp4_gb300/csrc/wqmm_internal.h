@@ -91,4 +91,21 @@ bool gemm_supports(const GemvArgs& a);
 // at least half of the SMs).
 bool gemm_prefers_light(const GemvArgs& a);
 
+// ---- NVFP4 x NVFP4 block-scaled tcgen05 GEMM (wqmm_gemm_f4f4.cu) ----
+struct F4F4Args {
+  const uint8_t* A;        // activation codes [M, K/2]
+  const uint8_t* A_scale;  // activation block scales [M, K/16], E4M3
+  const uint8_t* B;        // weight codes [N, K/2]
+  const uint8_t* ws;       // weight block scales [N, K/16], E4M3
+  const float* gscale;     // weight_scale_2 (device)
+  const void* bias;
+  void* Y;
+  int64_t M, N, K;
+  int dtype;
+};
+// Returns kUnsupported if the device or the shape cannot take this path
+// (K % 256 != 0).
+int launch_gemm_f4f4(const F4F4Args& a, cudaStream_t st);
+bool gemm_f4f4_supports(const F4F4Args& a);
+
 }  // namespace wqmm

@@ -263,6 +263,34 @@ int fp4_quantize_dequantize_activation(const void* A, void* out, int64_t M, int6
                                        void* stream);
 
 /*
+ * fp4_fp4_matmul -- Y = A_q * B_q^T (+ bias) with BOTH operands in NVFP4,
+ * steps 2-3 of the native FP4 x FP4 path of [FP4] §6 (step 1 is
+ * fp4_quantize_activation):
+ *     Y[m, n] = weight_scale_2 * sum_k e2m1(A_packed[m, k]) e4m3(A_scale[m, k/16])
+ *                                    * e2m1(B_packed[n, k]) e4m3(weight_scale[n, k/16])
+ *               (+ bias[n]), one RNE to dtype.
+ * Runs on the block-scaled tensor-core MMA (tcgen05.mma.kind::mxf4nvf4):
+ * products are exact, sums are FP32.
+ *   A_packed      [M, K/2] uint8, two E2M1 codes per byte (even k low), as
+ *                 written by fp4_quantize_activation.
+ *   A_scale       [M, K/16] uint8 E4M3 block scales of A.
+ *   B_packed, weight_scale, weight_scale_2, bias   the NVFP4 weight of
+ *                 fp4_weight_matmul with block_size 16.
+ *   Y             [M, N] dtype (dtype selects only the output and bias type).
+ * Block scales are read as unsigned E4M3 (the tensor core's scale type): the
+ * sign bit must be clear and 0x7F (NaN) is not allowed; the quantizer's
+ * scales always qualify.  K must be a multiple of 256 (WQMM_ERR_UNSUPPORTED
+ * otherwise); K == 0 writes Y = bias (or 0).
+ * Errors: odd K, a size < 0 or a NULL pointer -> INVALID_ARG; a pointer not
+ * 16-byte aligned (weight_scale_2 4, bias 2) -> MISALIGNED.
+ * Accuracy: the bound of fp4_weight_matmul with sum_k |A_q * B_dq| in place
+ * of sum_k |A * B_dq| (A_q = e2m1 * e4m3 of the codes).
+ */
+int fp4_fp4_matmul(const uint8_t* A_packed, const uint8_t* A_scale, const uint8_t* B_packed,
+                   const uint8_t* weight_scale, const float* weight_scale_2, const void* bias,
+                   void* Y, int64_t M, int64_t N, int64_t K, int dtype, void* stream);
+
+/*
  * fp4_dequantize -- expand an NVFP4 weight to the activation type.
  * [FP4] §2 formula, §5 step 1; [BLOG] vectorised dequant.
  *   out[n, k] = RNE_dtype( fp32( fp32(e2m1 * e4m3) * weight_scale_2 ) )

@@ -177,3 +177,23 @@ def test_noalloc_host_checks(L):
     assert f(asc=None) == 1
     assert f(Y=FAKE_ODD) == 3
     assert f(M=0, A=None, Y=None) == 0                   # empty output: no launch
+
+
+def test_fp4_fp4_matmul_host_checks(L):
+    """fp4_fp4_matmul: argument errors are reported before any CUDA call."""
+    def f(M=16, N=32, K=256, dt=1, A=FAKE, As=FAKE, B=FAKE, Ws=FAKE, g=FAKE, bias=None, Y=FAKE):
+        return L.fp4_fp4_matmul(A, As, B, Ws, g, bias, Y, M, N, K, dt, None)
+    assert f(dt=3) == 1
+    assert f(K=255) == 1              # odd K
+    assert f(M=-1) == 1
+    assert f(K=128) == 2              # K must be a multiple of 256
+    assert f(K=1 << 31) == 2
+    assert f(A=None) == 1
+    assert f(As=None) == 1
+    assert f(g=None) == 1
+    assert f(Y=None) == 1
+    assert f(Ws=FAKE_ODD) == 3
+    assert f(As=FAKE_ODD) == 3
+    assert f(bias=FAKE_ODD) == 3
+    assert f(M=0, A=None, Y=None) == 0
+    assert f(N=0, B=None, Y=None) == 0

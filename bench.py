@@ -529,6 +529,25 @@ def bench_also(gpu, args, peaks):
                                            "ms": round(dt_w * 1e3, 3),
                                            "vs_weight_only": round(dt / dt_w, 3)}
     del B8, s8, A, Y, ws, a_sc
+    # FP4 x FP4 prefill: the activation quantized to NVFP4 (timed separately
+    # and together with the GEMM), then the block-scaled tensor-core GEMM.
+    ly = gpu.fp4_layers(M, N, K, 1, seed0=700, bias=True)[0]
+    A = torch.randn(M, K, device=gpu.dev, dtype=torch.bfloat16)
+    qc, qs = wq.fp4_quantize_activation(A)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=gpu.dev)
+    gemm = lambda: wq.fp4_fp4_matmul(qc, qs, ly["B"], ly["ws"], ly["ws2"], ly["bias"], out=Y,
+                                     stream=gpu.stream)
+    both = lambda: (wq.fp4_quantize_activation(A, out_packed=qc, out_scale=qs, stream=gpu.stream),
+                    gemm())
+    dt = gpu.time_each(gemm, reps=5, warmup=2)
+    dt_q = gpu.time_each(both, reps=5, warmup=2)
+    tf = 2 * M * N * K / dt / 1e12
+    fp4_peak = 6 * tf_peak   # measured BF16 peak x the nominal FP4 : BF16 dense ratio
+    out[f"f4f4_prefill_M{M}_N{N}_K{K}"] = {"TFLOP/s": round(tf, 1), "frac": round(tf / fp4_peak, 4),
+                                           "peak_TFLOP/s": round(fp4_peak, 1),
+                                           "ms": round(dt * 1e3, 3),
+                                           "ms_with_activation_quantize": round(dt_q * 1e3, 3)}
+    del ly, A, qc, qs, Y
     return out
 
 

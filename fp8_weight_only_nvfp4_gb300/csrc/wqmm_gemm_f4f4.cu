@@ -13,22 +13,33 @@
 // the weight scales into that kernel's layout; here the scales keep the plain
 // [rows, K/16] layout of the weight format and are rearranged on chip.
 //
-// Tile: 128 weight rows (MMA M) x 256 tokens (MMA N) per CTA; K in stages of
-// 256 (one 128-byte swizzled row of packed codes per operand row), four MMAs
-// of K = 64 per stage.
-// Roles (10 warps):
-//   warp 0     TMA producer: per stage the packed weight tile [128 x 128 B] and
-//              activation tile [256 x 128 B] (K-major, 128-byte swizzle) and
-//              their scale tiles [128 x 16 B] and [256 x 16 B];
-//   warp 1     TMEM owner and MMA issuer (one elected thread);
-//   warps 2-9  scale writers, then the epilogue: warp w serves TMEM lane
-//              quarter w % 4 and takes every other stage; it moves the
-//              stage's scale bytes from shared memory to tensor memory in the
-//              layout the block-scaled MMA reads (below) with tcgen05.st.
-//              After the main loop: TMEM -> registers, * weight_scale_2,
-//              + bias, one RNE, Y through a shared-memory transpose and one
-//              tensor store (direct stores when the row pitch of Y is not a
-//              16-byte multiple).
+// Tile: 128 weight rows (MMA M) x 256 tokens (MMA N); K in stages of 256
+// (one 128-byte swizzled row of packed codes per operand row), four MMAs of
+// K = 64 per stage.  Persistent: one CTA per SM walks the tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (weight-row tiles fastest), and its stage ring,
+// scale writers and MMA run on without a break from one tile to the next; only
+// the first MMA of a tile waits until the epilogue warps have read the
+// previous tile's accumulator out of tensor memory.  (Measured at M = 8192,
+// N = 17408: one CTA per tile paid about 6 us per tile outside the main loop
+// -- start-up, pipeline fill, epilogue -- 42 % of the time at K = 5120.  A
+// cluster of 2 or 4 CTAs sharing the token tile through multicast copies, which
+// cuts the L2 traffic per SM by a third or a half, was 13 % / 18 % slower.)
+// Roles (14 warps):
+//   warp 0      TMA producer: per stage the packed weight tile [128 x 128 B]
+//               and activation tile [256 x 128 B] (K-major, 128-byte swizzle)
+//               and their scale tiles [128 x 16 B] and [256 x 16 B];
+//   warp 1      TMEM owner and MMA issuer (one elected thread);
+//   warps 2-5   scale writers: warp w serves TMEM lane quarter w % 4 and moves
+//               every stage's scale bytes from shared memory to tensor memory
+//               in the layout the block-scaled MMA reads (below) with
+//               tcgen05.st (one or two writer warps per quarter measured the
+//               same);
+//   warps 6-13  epilogue: warp w serves lane quarter w % 4 and half of the 256
+//               token columns: TMEM -> registers, * weight_scale_2, + bias, one
+//               RNE into packed pairs; it hands the accumulator back after its
+//               last tensor-memory load and only then stores to Y (lanes =
+//               consecutive weight rows n, 64 bytes per warp store).  Handing
+//               it back before the stores: 349 -> 324 us at M = 8192.
 //
 // Scale factors in tensor memory (scale_vec::4X): one 32-bit cell per operand
 // row and 64-k chunk, byte i holding the scale of the chunk's i-th 16-element
@@ -40,7 +51,7 @@
 // Every mbarrier wait is bounded; a wait that runs out raises a CTA-wide
 // abort flag, records WQMM_ERR_TIMEOUT and all roles drain to the TMEM
 // release at the end.
-#include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "wqmm_tcgen05.cuh"
@@ -55,9 +66,11 @@ constexpr int kBK = 256;              // k per stage
 constexpr int kRowBytes = kBK / 2;    // packed bytes per operand row per stage
 constexpr int kScBytes = kBK / 16;    // scale bytes per operand row per stage
 constexpr int kStages = 4;
-constexpr int kPh = 2;                // scale-writer warps per TMEM lane quarter
+constexpr int kPh = 1;                // scale-writer warps per TMEM lane quarter
 constexpr int kWriters = 4 * kPh;
-constexpr int kThreads = (2 + kWriters) * 32;
+constexpr int kEpi = 8;               // epilogue warps: 4 lane quarters x 2 column halves
+constexpr int kWarpEpi0 = 2 + kWriters;
+constexpr int kThreads = (2 + kWriters + kEpi) * 32;
 constexpr int kTmemCols = 512;
 
 // Shared memory (offsets from a 1024-byte aligned base).
@@ -73,12 +86,12 @@ constexpr int kOffFull = kOffWSc + kStages * kWSc;
 constexpr int kOffEmpty = kOffFull + 8 * kStages;
 constexpr int kOffReady = kOffEmpty + 8 * kStages;
 constexpr int kOffAcc = kOffReady + 8 * kStages;
-constexpr int kOffSlot = kOffAcc + 8;
+constexpr int kOffAccEmpty = kOffAcc + 8;
+constexpr int kOffSlot = kOffAccEmpty + 8;
 constexpr int kOffAbort = kOffSlot + 4;
 constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
 constexpr uint32_t kStageBytes = kActTile + kWTile + kActSc + kWSc;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-static_assert(kBN * kBM * 2 <= kStages * kActTile, "Y staging fits in the activation ring");
 static_assert(kStages % kPh == 0, "a writer's parity wait follows its own previous wait");
 
 // Tensor memory: accumulator [0, 256); per stage the token scales (8 columns
@@ -120,9 +133,9 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f4f4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmAS, const __grid_constant__ CUtensorMap tmWS,
-                     const __grid_constant__ CUtensorMap tmY, int y_tma,
                      const float* __restrict__ gscale, const uint16_t* __restrict__ bias,
-                     uint16_t* __restrict__ Y, int M, int N, int K, int* err) {
+                     uint16_t* __restrict__ Y, int M, int N, int K, int tiles_n, int tiles,
+                     int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -130,22 +143,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kOffEmpty);
   uint64_t* ready = reinterpret_cast<uint64_t*>(smem + kOffReady);
   uint64_t* accfull = reinterpret_cast<uint64_t*>(smem + kOffAcc);
+  uint64_t* accempty = reinterpret_cast<uint64_t*>(smem + kOffAccEmpty);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBM;
-  const int m0 = blockIdx.y * kBN;
   const int num_k = K / kBK;
+  // This CTA's tiles: blockIdx.x + i * gridDim.x for i < my_tiles.
+  const int my_tiles = (int)blockIdx.x < tiles
+                           ? (tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                           : 0;
+  const int total = my_tiles * num_k;  // stages this CTA runs
+  auto tile_n0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) % tiles_n * kBM; };
+  auto tile_m0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) / tiles_n * kBN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&ready[s], 4);  // one writer warp per lane quarter
+      mbar_init(&ready[s], 4);   // one writer warp per lane quarter
     }
     mbar_init(accfull, 1);
+    mbar_init(accempty, kEpi);   // every epilogue warp has read its columns
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -160,24 +180,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  bool have = false;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int issued = 0;
-      for (int it = 0; it < num_k; ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !wait_bar(&empty[s], ((it / kStages) + 1) & 1, err, abort_flag)) break;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(smem + kOffAct + s * kActTile, &tmA, it * kRowBytes, m0, &full[s]);
-        tma_load_2d(smem + kOffW + s * kWTile, &tmW, it * kRowBytes, n0, &full[s]);
-        tma_load_2d(smem + kOffActSc + s * kActSc, &tmAS, it * kScBytes, m0, &full[s]);
-        tma_load_2d(smem + kOffWSc + s * kWSc, &tmWS, it * kScBytes, n0, &full[s]);
-        ++issued;
+      int g = 0;  // stages issued so far (ring slot g % kStages, fill g / kStages)
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int n0 = tile_n0(i), m0 = tile_m0(i);
+        for (int k = 0; k < num_k; ++k, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !wait_bar(&empty[s], ((g / kStages) + 1) & 1, err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(smem + kOffAct + s * kActTile, &tmA, k * kRowBytes, m0, &full[s]);
+          tma_load_2d(smem + kOffW + s * kWTile, &tmW, k * kRowBytes, n0, &full[s]);
+          tma_load_2d(smem + kOffActSc + s * kActSc, &tmAS, k * kScBytes, m0, &full[s]);
+          tma_load_2d(smem + kOffWSc + s * kWSc, &tmWS, k * kScBytes, n0, &full[s]);
+        }
       }
       // No copy may still be landing in shared memory when the CTA exits.
-      for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it)
+      for (int it = (g > kStages ? g - kStages : 0); it < g; ++it)
         drain_wait(&full[it % kStages], (it / kStages) & 1);
     }
   } else if (warp == 1) {
@@ -187,42 +212,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       int committed = -1;
       const uint64_t adesc0 = desc_kmajor_sw128(smem_u32(smem + kOffW));
       const uint64_t bdesc0 = desc_kmajor_sw128(smem_u32(smem + kOffAct));
-      for (int it = 0; it < num_k; ++it) {
-        const int s = it % kStages;
-        // ready[s] implies full[s]: each writer warp arrives only after its
-        // own wait on full[s], which covers all four copies of the stage.
-        if (!wait_bar(&ready[s], (it / kStages) & 1, err, abort_flag)) {
+      int g = 0;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        // The accumulator is free once the epilogue has read tile i - 1.
+        if (i > 0 && !wait_bar(accempty, (i - 1) & 1, err, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        mma_f4_stage(tmem + kColAcc, adesc0 + (uint64_t)((s * kWTile) >> 4),
-                     bdesc0 + (uint64_t)((s * kActTile) >> 4), tmem + kColSfa + 16 * s,
-                     tmem + kColSfb + 32 * s, it > 0 ? 1u : 0u);
-        mma_commit(&empty[s]);
-        committed = it;
+        for (int k = 0; k < num_k; ++k, ++g) {
+          const int s = g % kStages;
+          // ready[s] implies full[s]: each writer warp arrives only after its
+          // own wait on full[s], which covers all four copies of the stage.
+          if (!wait_bar(&ready[s], (g / kStages) & 1, err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_f4_stage(tmem + kColAcc, adesc0 + (uint64_t)((s * kWTile) >> 4),
+                       bdesc0 + (uint64_t)((s * kActTile) >> 4), tmem + kColSfa + 16 * s,
+                       tmem + kColSfb + 32 * s, k > 0 ? 1u : 0u);
+          mma_commit(&empty[s]);
+          committed = g;
+        }
+        if (ok) mma_commit(accfull);  // tile i's accumulator is complete
       }
-      if (ok) {
-        mma_commit(accfull);
-      } else if (committed >= 0) {
+      if (!ok && committed >= 0) {
         // MMAs still reading tensor memory must finish before the release.
         drain_wait(&empty[committed % kStages], (committed / kStages) & 1);
       }
     }
-  } else {
-    // ---------------- scale writers, then the epilogue ----------------
+  } else if (warp < kWarpEpi0) {
+    // ---------------- scale writers ----------------
     const int q = warp & 3;               // TMEM lane quarter
     const int ph = (warp - 2) >> 2;       // stage phase of this warp
-    const int row = q * 32 + lane;        // weight row within the tile
-    const int n = n0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    bool ok = true;
-    for (int it = ph; it < num_k; it += kPh) {
-      const int s = it % kStages;
-      if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) {
-        ok = false;
-        break;
-      }
+    for (int g = ph; g < total; g += kPh) {
+      const int s = g % kStages;
+      if (!wait_bar(&full[s], (g / kStages) & 1, err, abort_flag)) break;
       // Register j of the weight-scale store goes to column j: chunk j / 4,
       // row group j % 4 (rows 32 (j % 4) + lane); the token-scale store has 8
       // columns per chunk, row group (j % 8) of 32 tokens.
@@ -252,42 +279,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ready[s]);
     }
-    // Epilogue: this warp's lane quarter, token-column chunks of 32 taken in
-    // turn by the quarter's kPh warps.
-    have = ok && wait_bar(accfull, 0, err, abort_flag) && !*abort_flag;
-    if (have) {
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;                   // TMEM lane quarter
+    const int h = (warp - kWarpEpi0) >> 2;    // token-column half
+    const int row = q * 32 + lane;            // weight row within the tile
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const float gs = __ldg(gscale);
+    for (int i = 0; i < my_tiles; ++i) {
+      if (!wait_bar(accfull, i & 1, err, abort_flag)) break;
       tc_fence_after();
-      const float gs = __ldg(gscale);
+      const int n = tile_n0(i) + row, m0 = tile_m0(i);
       const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
-      uint16_t* stage_y = reinterpret_cast<uint16_t*>(smem + kOffAct);
-#pragma unroll 1
-      for (int c0 = 32 * ph; c0 < kBN; c0 += 32 * kPh) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + kColAcc + c0, r);
-        if (y_tma) {
+      // The warp's 128 columns leave tensor memory 16 at a time and stay in
+      // registers as packed output pairs, so the accumulator is handed back
+      // before any store is issued.
+      uint32_t pk[kBN / 64][16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            stage_y[(c0 + j) * kBM + row] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
-        } else if (n < N) {
+      for (int c = 0; c < kBN / 64; ++c) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = m0 + c0 + j;
-            if (m < M) Y[(int64_t)m * N + n] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
-          }
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[16];
+          tmem_ld16(lane_base + kColAcc + 64 * c + 32 * h + 16 * half, r);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[c][8 * half + j] = pack2_rn<DT>(__uint_as_float(r[2 * j]) * gs + b,
+                                               __uint_as_float(r[2 * j + 1]) * gs + b);
         }
       }
-    }
-    if (y_tma) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      asm volatile("bar.sync 1, %0;" ::"n"(kWriters * 32) : "memory");
-      if (have && warp == 2 && lane == 0 && !*abort_flag) {
-        asm volatile(
-            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                reinterpret_cast<uint64_t>(&tmY)),
-            "r"(n0), "r"(m0), "r"(smem_u32(smem + kOffAct))
-            : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty);
+      if (n < N) {
+        // Token rows m0 + 64 c + 32 h + t, t < 32, in order, one running pointer.
+        uint16_t* yp = Y + (int64_t)(m0 + 32 * h) * N + n;
+        int m = m0 + 32 * h;
+#pragma unroll
+        for (int c = 0; c < kBN / 64; ++c) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (m < M) *yp = (uint16_t)(pk[c][j] & 0xFFFFu);
+            yp += N;
+            if (m + 1 < M) *yp = (uint16_t)(pk[c][j] >> 16);
+            yp += N;
+            m += 2;
+          }
+          yp += (int64_t)32 * N;  // the other half's 32 tokens
+          m += 32;
+        }
       }
     }
   }
@@ -304,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DT>
 int launch_t(const F4F4Args& a, cudaStream_t st) {
   const uint64_t rowb = (uint64_t)a.K / 2, scb = (uint64_t)a.K / 16;
-  CUtensorMap tmA, tmW, tmAS, tmWS, tmY;
+  CUtensorMap tmA, tmW, tmAS, tmWS;
   if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, rowb, (uint64_t)a.M, rowb,
                       kRowBytes, kBN, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
@@ -317,15 +356,6 @@ int launch_t(const F4F4Args& a, cudaStream_t st) {
       !encode_tmap_2d(&tmWS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ws, scb, (uint64_t)a.N, scb,
                       kScBytes, kBM, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return kCuda;
-  const CUtensorMapDataType ydt =
-      DT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  int y_tma = 0;
-  std::memset(&tmY, 0, sizeof(tmY));
-  if (a.N % 8 == 0)
-    y_tma = encode_tmap_2d(&tmY, ydt, a.Y, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.N * 2, kBM,
-                           kBN, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
-                ? 1
-                : 0;
   static std::once_flag once[64];
   const int dev = device_info().device;
   if (dev < 0 || dev >= 64) return kCuda;
@@ -333,10 +363,13 @@ int launch_t(const F4F4Args& a, cudaStream_t st) {
     cudaFuncSetAttribute(gemm_f4f4_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          kSmemBytes);
   });
-  const dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)((a.M + kBN - 1) / kBN), 1);
+  const int64_t tiles_n = (a.N + kBM - 1) / kBM;
+  const int64_t tiles = tiles_n * ((a.M + kBN - 1) / kBN);
+  const int grid = (int)std::min<int64_t>(tiles, device_info().sm_count);
   gemm_f4f4_kernel<DT><<<grid, kThreads, kSmemBytes, st>>>(
-      tmA, tmW, tmAS, tmWS, tmY, y_tma, a.gscale, reinterpret_cast<const uint16_t*>(a.bias),
-      reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, device_error_word());
+      tmA, tmW, tmAS, tmWS, a.gscale, reinterpret_cast<const uint16_t*>(a.bias),
+      reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, (int)tiles_n, (int)tiles,
+      device_error_word());
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 
@@ -346,7 +379,9 @@ bool gemm_f4f4_supports(const F4F4Args& a) {
   const DeviceInfo& d = device_info();
   if (d.cc_major != 10 || d.max_smem_optin < kSmemBytes) return false;
   if (a.K % kBK != 0) return false;
-  return (a.M + kBN - 1) / kBN <= 65535 && a.N < (int64_t(1) << 31);
+  // Tile indices are int.
+  const int64_t tiles = ((a.N + kBM - 1) / kBM) * ((a.M + kBN - 1) / kBN);
+  return tiles < (int64_t(1) << 31) && a.N < (int64_t(1) << 31);
 }
 
 int launch_gemm_f4f4(const F4F4Args& a, cudaStream_t st) {

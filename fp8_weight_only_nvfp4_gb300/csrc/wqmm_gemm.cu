@@ -50,6 +50,7 @@
 // Every mbarrier wait is bounded; a wait that runs out raises a CTA-wide
 // abort flag, records WQMM_ERR_TIMEOUT, and all roles drain to the TMEM
 // release at the end.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -113,7 +114,8 @@ struct GemmCfg {
   static constexpr int empty = full + 8 * stages;
   static constexpr int afull = empty + 8 * stages;
   static constexpr int accfull = afull + 8 * stages;
-  static constexpr int tmem_slot = accfull + 8;
+  static constexpr int accempty = accfull + 8;   // persistent kernel only
+  static constexpr int tmem_slot = accempty + 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int total = abort_flag + 4;
   static constexpr int smem_bytes = total + 1024;  // + alignment slack
@@ -181,6 +183,138 @@ __device__ __forceinline__ void decode_fp4_word(uint32_t w, uint32_t sc16, uint3
   for (int i = 0; i < 4; ++i) out[i] = fold_f16x2<DT>(h[i], sc2);
 }
 
+// One decoder thread's weight row n over the K range [k_lo, k_lo + num_k)
+// stages: its block scales, fetched a turn ahead of use, and the decode of
+// one 64-k stage of its packed codes (from the stage's shared-memory weight
+// tile) into 32 words of 16-bit MMA operands.
+template <int DT, int KIND>
+struct RowDecoder {
+  const uint8_t* ws_row;
+  const float* fs_row;
+  int n, N, K, bs, bs_shift, k_lo, num_k;
+  // With 16-element blocks and a scale row length that is a multiple of 4,
+  // a stage's four scale bytes are one aligned word, all of it in range.
+  bool scale_word;
+  // FP8 with blocks of 64 or more k: one scale for the whole stage.
+  bool scale_one;
+  // FP8 weights with FP16 activations: the folded operand e4m3 * b_scale has
+  // to stay inside the FP16 range whatever b_scale is (448 * 147 already
+  // overflows it).  A decoder thread owns one weight row over its K range, so
+  // it divides that row's block scales by the power of two 2^E that brings
+  // their largest magnitude into [1, 2) -- exact -- and its accumulator is
+  // multiplied by row_pow2 = 2^E afterwards, also exact: every operand then
+  // lies within 448 * 2.  1 otherwise.
+  float scale_norm, row_pow2;
+
+  __device__ __forceinline__ void init(const uint8_t* ws, const float* fscale, int n_, int N_,
+                                       int K_, int bs_, int k_lo_, int num_k_) {
+    n = n_;
+    N = N_;
+    K = K_;
+    bs = bs_;
+    k_lo = k_lo_;
+    num_k = num_k_;
+    const int S = (K + bs - 1) / bs;
+    bs_shift = ((bs & (bs - 1)) == 0) ? __ffs(bs) - 1 : -1;
+    ws_row = ws + (int64_t)n * S;
+    fs_row = fscale + (int64_t)n * S;
+    scale_word = KIND == 0 && bs == 16 && (S & 3) == 0;
+    scale_one = KIND == 1 && (bs & 63) == 0;
+    scale_norm = 1.0f;
+    row_pow2 = 1.0f;
+    if constexpr (KIND == 1 && DT == 0) {
+      float rmax = 0.f;
+      if (n < N) {
+        const int k_begin = k_lo * kBK, k_end = min(K, (k_lo + num_k) * kBK);
+        const int c0 = bs_shift >= 0 ? k_begin >> bs_shift : k_begin / bs;
+        const int c1 = bs_shift >= 0 ? (k_end - 1) >> bs_shift : (k_end - 1) / bs;
+        for (int c = c0; c <= c1; ++c) rmax = fmaxf(rmax, fabsf(__ldg(fs_row + c)));
+      }
+      // floor(log2(rmax)) for a normal rmax; zero, subnormal, inf and NaN
+      // maxima keep E = 0.
+      const int e = (int)((__float_as_uint(rmax) >> 23) & 0xFFu) - 127;
+      const int ec = (e >= -126 && e <= 126) ? e : 0;
+      scale_norm = __uint_as_float((uint32_t)(127 - ec) << 23);
+      row_pow2 = __uint_as_float((uint32_t)(127 + ec) << 23);
+    }
+  }
+
+  // Raw scales of the four 16-k chunks of stage `it` (bs is a multiple of 16);
+  // zeros past the range.
+  __device__ __forceinline__ void fetch(int it, uint32_t (&r)[4]) const {
+    if (scale_one) {
+      const int k0 = (k_lo + it) * kBK;
+      uint32_t v = 0u;
+      if (n < N && it < num_k && k0 < K) {
+        const int col = bs_shift >= 0 ? k0 >> bs_shift : k0 / bs;
+        v = __float_as_uint(__ldg(fs_row + col));
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) r[c] = v;
+      return;
+    }
+    if (scale_word) {
+      const int k0 = (k_lo + it) * kBK;
+      uint32_t w = 0u;
+      if (n < N && it < num_k && k0 < K)
+        w = __ldg(reinterpret_cast<const uint32_t*>(ws_row + (k0 >> 4)));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) r[c] = (w >> (8 * c)) & 0xFFu;
+      return;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int k1 = (k_lo + it) * kBK + 16 * c;
+      r[c] = 0u;
+      if (n < N && it < num_k && k1 < K) {
+        const int col = bs_shift >= 0 ? k1 >> bs_shift : k1 / bs;
+        if constexpr (KIND == 0)
+          r[c] = __ldg(ws_row + col);
+        else
+          r[c] = __float_as_uint(__ldg(fs_row + col));
+      }
+    }
+  }
+
+  // Decodes this thread's weight row `row` of the stage tile `wt` with the
+  // stage's scales `sc`.
+  __device__ __forceinline__ void decode(const uint8_t* wt, int row, const uint32_t (&sc)[4],
+                                         uint32_t (&v)[32]) const {
+    if constexpr (KIND == 0) {
+      // The row's 32-byte stage run (64 k), 32-byte swizzle.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t off = row * 32 + 16 * h;
+        const uint32_t phys = off ^ (((off >> 7) & 1u) << 4);
+        const uint4 pw = *reinterpret_cast<const uint4*>(wt + phys);
+        const uint32_t sa = e4m3x2_to_f16x2(sc[2 * h]) & 0xFFFFu;
+        const uint32_t sb = e4m3x2_to_f16x2(sc[2 * h + 1]) & 0xFFFFu;
+        decode_fp4_word<DT>(pw.x, sa, &v[16 * h + 0]);
+        decode_fp4_word<DT>(pw.y, sa, &v[16 * h + 4]);
+        decode_fp4_word<DT>(pw.z, sb, &v[16 * h + 8]);
+        decode_fp4_word<DT>(pw.w, sb, &v[16 * h + 12]);
+      }
+    } else {
+      // The row's 64-byte stage run (64 k), 64-byte swizzle.
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 p = lds_swz<3>(wt, row * 64 + 16 * c);
+        const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+        float scf = __uint_as_float(sc[c]);
+        if constexpr (DT == 0) scf *= scale_norm;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float2 e = f16x2_to_f32x2(e4m3x2_to_f16x2((w4[i] >> (16 * h)) & 0xFFFFu));
+            v[8 * c + 2 * i + h] = pack2_rn<DT>(e.x * scf, e.y * scf);
+          }
+        }
+      }
+    }
+  }
+};
+
 // KIND 0 = NVFP4 weight, 1 = FP8 weight.  DT 0 = FP16, 1 = BF16.  BN =
 // tokens per tile (MMA N).
 template <int DT, int KIND, int BN, int PH>
@@ -216,7 +350,6 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
   const int spc = (num_k_all + C - 1) / C;
   const int k_lo = rank * spc;
   const int num_k = min(num_k_all, k_lo + spc) - k_lo;
-  const int S = (K + bs - 1) / bs;
   constexpr int kWBytes = (KIND == 0) ? kBK / 2 : kBK;  // packed bytes per row per stage
 
   if (threadIdx.x == 0) {
@@ -324,121 +457,25 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
     const int row = q * 32 + lane;          // weight row within the tile
     const int n = n0 + row;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    const int bs_shift = ((bs & (bs - 1)) == 0) ? __ffs(bs) - 1 : -1;
-    const uint8_t* ws_row = ws + (int64_t)n * S;
-    const float* fs_row = fscale + (int64_t)n * S;
-    // Raw scales of the four 16-k chunks of stage `it` (bs is a multiple of
-    // 16), fetched one turn (four stages) ahead of their use.
-    // With 16-element blocks and a scale row length that is a multiple of 4,
-    // a stage's four scale bytes are one aligned word, all of it in range.
-    const bool scale_word = KIND == 0 && bs == 16 && (S & 3) == 0;
-    // FP8 with blocks of 64 or more k: one scale for the whole stage.
-    const bool scale_one = KIND == 1 && (bs & 63) == 0;
-    auto fetch = [&](int it, uint32_t (&r)[4]) {
-      if (scale_one) {
-        const int k0 = (k_lo + it) * kBK;
-        uint32_t v = 0u;
-        if (n < N && it < num_k && k0 < K) {
-          const int col = bs_shift >= 0 ? k0 >> bs_shift : k0 / bs;
-          v = __float_as_uint(__ldg(fs_row + col));
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) r[c] = v;
-        return;
-      }
-      if (scale_word) {
-        const int k0 = (k_lo + it) * kBK;
-        uint32_t w = 0u;
-        if (n < N && it < num_k && k0 < K)
-          w = __ldg(reinterpret_cast<const uint32_t*>(ws_row + (k0 >> 4)));
-#pragma unroll
-        for (int c = 0; c < 4; ++c) r[c] = (w >> (8 * c)) & 0xFFu;
-        return;
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int k1 = (k_lo + it) * kBK + 16 * c;
-        r[c] = 0u;
-        if (n < N && it < num_k && k1 < K) {
-          const int col = bs_shift >= 0 ? k1 >> bs_shift : k1 / bs;
-          if constexpr (KIND == 0)
-            r[c] = __ldg(ws_row + col);
-          else
-            r[c] = __float_as_uint(__ldg(fs_row + col));
-        }
-      }
-    };
-    // FP8 weights with FP16 activations: the folded operand e4m3 * b_scale
-    // has to stay inside the FP16 range whatever b_scale is (448 * 147
-    // already overflows it).  A decoder thread owns one weight row over the
-    // CTA's whole K range, so it divides that row's block scales by the
-    // power of two 2^E that brings their largest magnitude into [1, 2) --
-    // exact -- and its accumulator is multiplied by 2^E afterwards, also
-    // exact: every operand then lies within 448 * 2.
-    float scale_norm = 1.0f;
-    if constexpr (KIND == 1 && DT == 0) {
-      float rmax = 0.f;
-      if (n < N) {
-        const int k_begin = k_lo * kBK, k_end = min(K, (k_lo + num_k) * kBK);
-        const int c0 = bs_shift >= 0 ? k_begin >> bs_shift : k_begin / bs;
-        const int c1 = bs_shift >= 0 ? (k_end - 1) >> bs_shift : (k_end - 1) / bs;
-        for (int c = c0; c <= c1; ++c) rmax = fmaxf(rmax, fabsf(__ldg(fs_row + c)));
-      }
-      // floor(log2(rmax)) for a normal rmax; zero, subnormal, inf and NaN
-      // maxima keep E = 0.
-      const int e = (int)((__float_as_uint(rmax) >> 23) & 0xFFu) - 127;
-      const int ec = (e >= -126 && e <= 126) ? e : 0;
-      scale_norm = __uint_as_float((uint32_t)(127 - ec) << 23);
-      row_pow2 = __uint_as_float((uint32_t)(127 + ec) << 23);
-    }
+    RowDecoder<DT, KIND> rd;
+    rd.init(ws, fscale, n, N, K, bs, k_lo, num_k);
+    row_pow2 = rd.row_pow2;
     uint32_t scn[4];
-    fetch(j4, scn);  // (j4 = this warp's stage phase, 0 .. kPh - 1)
+    rd.fetch(j4, scn);  // (j4 = this warp's stage phase, 0 .. kPh - 1)
     bool ok = true;
     for (int it = j4; it < num_k; it += kPh) {
       const int s = it % kStages;
       uint32_t sc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) sc[c] = scn[c];
-      fetch(it + kPh, scn);
+      rd.fetch(it + kPh, scn);
       if (!wait_bar(&full[s], (it / kStages) & 1, err, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint8_t* wt = smem + L::w + s * L::wstage;
       uint32_t v[32];
-      if constexpr (KIND == 0) {
-        // The row's 32-byte stage run (64 k), 32-byte swizzle.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t off = row * 32 + 16 * h;
-          const uint32_t phys = off ^ (((off >> 7) & 1u) << 4);
-          const uint4 pw = *reinterpret_cast<const uint4*>(wt + phys);
-          const uint32_t sa = e4m3x2_to_f16x2(sc[2 * h]) & 0xFFFFu;
-          const uint32_t sb = e4m3x2_to_f16x2(sc[2 * h + 1]) & 0xFFFFu;
-          decode_fp4_word<DT>(pw.x, sa, &v[16 * h + 0]);
-          decode_fp4_word<DT>(pw.y, sa, &v[16 * h + 4]);
-          decode_fp4_word<DT>(pw.z, sb, &v[16 * h + 8]);
-          decode_fp4_word<DT>(pw.w, sb, &v[16 * h + 12]);
-        }
-      } else {
-        // The row's 64-byte stage run (64 k), 64-byte swizzle.
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 p = lds_swz<3>(wt, row * 64 + 16 * c);
-          const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
-          float scf = __uint_as_float(sc[c]);
-          if constexpr (DT == 0) scf *= scale_norm;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float2 e = f16x2_to_f32x2(e4m3x2_to_f16x2((w4[i] >> (16 * h)) & 0xFFFFu));
-              v[8 * c + 2 * i + h] = pack2_rn<DT>(e.x * scf, e.y * scf);
-            }
-          }
-        }
-      }
+      rd.decode(smem + L::w + s * L::wstage, row, sc, v);
       tmem_st32(lane_base + L::a_col + s * (kBK / 2), v);
       tmem_st_wait();
       tc_fence_before();
@@ -581,6 +618,264 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
   }
 }
 
+// Persistent form of gemm_tc_kernel for the 256-token prefill tile without a
+// K split: one CTA per SM walks the tiles blockIdx.x, blockIdx.x + gridDim.x,
+// ... (weight-row tiles fastest).  Producer, decoders and MMA run on across
+// tile boundaries -- the producer keeps filling the ring with the next tile's
+// stages while the current one finishes -- and the decoders run each tile's
+// epilogue as soon as their own last stage of it is done: they read their
+// accumulator columns, hand the accumulator back to the MMA thread (the first
+// MMA of the next tile waits for that), store Y directly (lanes = consecutive
+// weight rows, 64 bytes per warp store) and go on decoding.  A CTA per tile
+// paid about 6 us per tile outside its main loop (start-up, pipeline fill and
+// an epilogue that overlapped nothing; a K sweep at M = 8192, N = 17408).
+template <int DT, int KIND, int PH>
+__global__ void __launch_bounds__(Shape<PH>::threads, 1)
+    gemm_tc_persist(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                    const uint8_t* __restrict__ ws, const float* __restrict__ gscale,
+                    const float* __restrict__ fscale, const uint16_t* __restrict__ bias,
+                    uint16_t* __restrict__ Y, int M, int N, int K, int bs, int tiles_n, int tiles,
+                    int* err) {
+  constexpr int BN = 256;
+  using L = GemmCfg<KIND, BN, PH>;
+  constexpr int kStages = L::stages;
+  constexpr int kPh = PH;
+  constexpr int kTmemCols = Shape<PH>::tmem_cols;
+  constexpr int kDec = Shape<PH>::dec_warps;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L::empty);
+  uint64_t* afull = reinterpret_cast<uint64_t*>(smem + L::afull);
+  uint64_t* accfull = reinterpret_cast<uint64_t*>(smem + L::accfull);
+  uint64_t* accempty = reinterpret_cast<uint64_t*>(smem + L::accempty);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort_flag);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_k = (K + kBK - 1) / kBK;
+  const int my_tiles = (int)blockIdx.x < tiles
+                           ? (tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                           : 0;
+  auto tile_n0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) % tiles_n * kBM; };
+  auto tile_m0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) / tiles_n * BN; };
+  constexpr int kWBytes = (KIND == 0) ? kBK / 2 : kBK;  // packed bytes per row per stage
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&afull[s], 4);  // one decoder warp per lane quarter
+    }
+    mbar_init(accfull, 1);
+    mbar_init(accempty, kDec);  // every decoder warp has read its columns
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint32_t bytes = L::act_stage + kBM * kWBytes;
+      int g = 0;  // stages issued (ring slot g % kStages, fill g / kStages)
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int n0 = tile_n0(i), m0 = tile_m0(i);
+        for (int it = 0; it < num_k; ++it, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !wait_bar(&empty[s], ((g / kStages) + 1) & 1, err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_2d(smem + L::act + s * L::act_stage, &tmA, it * kBK, m0, &full[s]);
+          tma_load_2d(smem + L::w + s * L::wstage, &tmW, it * kWBytes, n0, &full[s]);
+        }
+      }
+      for (int it = (g > kStages ? g - kStages : 0); it < g; ++it)
+        drain_wait(&full[it % kStages], (it / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc<BN>(DT == 1 ? 1 : 0);
+      bool ok = true;
+      int committed = -1;
+      const uint64_t bdesc0 = desc_kmajor_sw128(smem_u32(smem + L::act));
+      const uint32_t afull0 = smem_u32(afull);
+      uint64_t bdesc = bdesc0;
+      uint32_t a_tmem = tmem + L::a_col;
+      int s = 0, g = 0;
+      uint32_t par = 0;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        // The accumulator is free once the decoders have read tile i - 1.
+        if (i > 0 && !wait_bar(accempty, (i - 1) & 1, err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int it = 0; it < num_k; ++it, ++g) {
+          if (!mbar_try_wait(afull0 + 8u * (uint32_t)s, par) &&
+              !wait_bar(&afull[s], par, err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_ts_stage(tmem + kAccCol, a_tmem, bdesc, idesc, it > 0 ? 1u : 0u);
+          mma_commit(&empty[s]);
+          committed = g;
+          if (++s == kStages) {
+            s = 0;
+            par ^= 1u;
+            bdesc = bdesc0;
+            a_tmem = tmem + L::a_col;
+          } else {
+            bdesc += (uint64_t)(L::act_stage >> 4);
+            a_tmem += kBK / 2;
+          }
+        }
+        if (ok) mma_commit(accfull);  // tile i's accumulator is complete
+      }
+      if (!ok && committed >= 0)
+        drain_wait(&empty[committed % kStages], (committed / kStages) & 1);
+    }
+  } else {
+    // ---------------- decoders, each tile's epilogue ----------------
+    // A warp that has finished its stages of tile i first decodes its first
+    // stage of tile i + 1 (those stages depend only on tile i's MMAs, never
+    // on its epilogue), then runs tile i's epilogue: when the accumulator is
+    // handed back, the MMA finds the next tile's first stages ready.
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int j4 = (warp - 2) >> 2;         // stage phase of this warp
+    const int row = q * 32 + lane;          // weight row within the tile
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const int total = my_tiles * num_k;
+    // Epilogue of tile e.
+    auto epilogue = [&](int e) -> bool {
+      if (!wait_bar(accfull, e & 1, err, abort_flag)) return false;
+      tc_fence_after();
+      const int n = tile_n0(e) + row, m0 = tile_m0(e);
+      float gs = 1.0f;
+      if constexpr (KIND == 0) {
+        gs = __ldg(gscale);
+      } else if constexpr (DT == 0) {
+        // The power of two this row's FP8 block scales were divided by.
+        RowDecoder<DT, KIND> t;
+        t.init(ws, fscale, n, N, K, bs, 0, num_k);
+        gs = t.row_pow2;
+      }
+      const float b = (bias != nullptr && n < N) ? act_to_f32<DT>(__ldg(bias + n)) : 0.0f;
+#pragma unroll 1
+      for (int c0 = 32 * j4; c0 < BN; c0 += 32 * kPh) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + kAccCol + c0, r);
+        if (c0 + 32 * kPh >= BN) {
+          // This warp's last read of the accumulator: hand it back.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(accempty);
+        }
+        if (n < N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < M) Y[(int64_t)m * N + n] = to_act_rn<DT>(__uint_as_float(r[j]) * gs + b);
+          }
+        }
+      }
+      return true;
+    };
+    RowDecoder<DT, KIND> rd;
+    int cur = -1;   // tile rd is set up for
+    int owed = 0;   // next tile whose epilogue this warp has not run
+    uint32_t scn[4];
+    bool ok = true;
+    for (int g = j4; g < total && ok; g += kPh) {
+      const int i = g / num_k, it = g - i * num_k;
+      if (i != cur) {
+        rd.init(ws, fscale, tile_n0(i) + row, N, K, bs, 0, num_k);
+        cur = i;
+        rd.fetch(it, scn);
+      }
+      const int s = g % kStages;
+      uint32_t sc[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sc[c] = scn[c];
+      rd.fetch(it + kPh, scn);
+      if (!wait_bar(&full[s], (g / kStages) & 1, err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[32];
+      rd.decode(smem + L::w + s * L::wstage, row, sc, v);
+      tmem_st32(lane_base + L::a_col + s * (kBK / 2), v);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[s]);  // one arrival per lane quarter
+      // Epilogues owed for the tiles before this stage's tile (more than one
+      // when a warp has no stage in some tile, num_k < kPh).
+      while (ok && owed < i) ok = epilogue(owed++);
+    }
+    while (ok && owed < my_tiles) ok = epilogue(owed++);
+  }
+
+  // Teardown: every tcgen05 access of this CTA is complete before the release.
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int DT, int KIND, int PH>
+int launch_persist(const GemvArgs& a, cudaStream_t st) {
+  constexpr int BN = 256;
+  const int wbytes_per_stage = (KIND == 0) ? kBK / 2 : kBK;
+  CUtensorMap tmA, tmW;
+  const CUtensorMapDataType adt =
+      DT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!encode_tmap_2d(&tmA, adt, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, kBK, BN,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    return kCuda;
+  const uint64_t wrow = (KIND == 0) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+  if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, wrow, (uint64_t)a.N, wrow,
+                      wbytes_per_stage, kBM,
+                      KIND == 0 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    return kCuda;
+  using L = GemmCfg<KIND, BN, PH>;
+  using SH = Shape<PH>;
+  static std::once_flag once[64];
+  const int dev = device_info().device;
+  if (dev < 0 || dev >= 64) return kCuda;
+  std::call_once(once[dev], [] {
+    cudaFuncSetAttribute(gemm_tc_persist<DT, KIND, PH>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
+  });
+  const int64_t tiles_n = (a.N + kBM - 1) / kBM;
+  const int64_t tiles = tiles_n * ((a.M + BN - 1) / BN);
+  const int grid = (int)std::min<int64_t>(tiles, device_info().sm_count);
+  gemm_tc_persist<DT, KIND, PH><<<grid, SH::threads, L::smem_bytes, st>>>(
+      tmA, tmW, a.ws, a.gscale, a.fscale, reinterpret_cast<const uint16_t*>(a.bias),
+      reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, a.bs, (int)tiles_n,
+      (int)tiles, device_error_word());
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
 template <int DT, int KIND, int BN, int PH>
 int launch_t(const GemvArgs& a, cudaStream_t st) {
   const int wbytes_per_stage = (KIND == 0) ? kBK / 2 : kBK;
@@ -693,7 +988,14 @@ int launch_bn(const GemvArgs& a, cudaStream_t st) {
     case 32: return launch_narrow<DT, KIND, 32>(a, st);
     case 64: return launch_narrow<DT, KIND, 64>(a, st);
     case 128: return launch_narrow<DT, KIND, 128>(a, st);
-    default: return launch_t<DT, KIND, 256, kFullPh256[KIND]>(a, st);
+    default: {
+      // Enough 256-token tiles to fill the GPU without a K split: the
+      // persistent kernel; fewer: one CTA per tile with a cluster K split.
+      const int64_t tiles = ((a.N + kBM - 1) / kBM) * ((a.M + 255) / 256);
+      if (tiles * 2 > device_info().sm_count)
+        return launch_persist<DT, KIND, kFullPh256[KIND]>(a, st);
+      return launch_t<DT, KIND, 256, kFullPh256[KIND]>(a, st);
+    }
   }
 }
 

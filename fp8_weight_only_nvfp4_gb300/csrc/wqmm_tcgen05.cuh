@@ -117,28 +117,6 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[N]) {
   else tmem_ld8(taddr, v);
 }
 
-// Like mma_commit, but the completion arrives on the barrier at `bar`'s offset in every
-// CTA of the cluster named in `cta_mask` (each of them counts one arrival).
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// 2-D tiled tensor load delivered to the same shared-memory offset in every
-// CTA of the cluster named in `cta_mask`; each destination's barrier at
-// `bar`'s offset receives the byte count of the tile.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* m, int x,
-                                                      int y, uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes."
-      "multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
 // 8-row core groups 1024 bytes apart (SBO), version field = 1 (sm_100 family).
 __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {

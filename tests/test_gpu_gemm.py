@@ -247,3 +247,51 @@ def test_gemm_repeated_runs_bit_identical(kind, M, N, K, bs):
     assert torch.isfinite(first.float()).all()
     for _ in range(9):
         assert torch.equal(run(), first)
+
+
+# ---------------------------------------------------------------------------
+# Persistent prefill kernel: 256-token tiles, enough of them to fill the GPU
+# without a K split (tiles * 2 > SMs); with more tiles than SMs some CTAs run
+# several tiles in turn, the stage ring and parities running on across them.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+@pytest.mark.parametrize("M,N,K,bs", [
+    (1000, 5000, 640, 16),     # 4 x 40 = 160 tiles: ragged last token and row tiles
+    (2048, 2560, 1024, 32),    # 8 x 20 = 160 tiles
+    (700, 4096, 320, 16),      # 3 x 32 = 96 tiles: one per CTA
+])
+def test_persistent_prefill_tiles(M, N, K, bs, dtype):
+    p = wl.make_fp4(M, N, K, bs, dtype, seed=M + N + K, bias_sigma=0.05)
+    assert_within_tolerance(run_fp4(p), *_ref(p), dtype, f"persistent {M}x{N}x{K} bs={bs}")
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+@pytest.mark.parametrize("K", [1024, 256])
+def test_persistent_fp8_tiles(dtype, K):
+    """FP8 weights through the persistent kernel (five decoder phases), 160
+    tiles, FP16 included (row scale normalisation per tile); K = 256 gives
+    four stages per tile, fewer than the decoder phases, so some decoder warps
+    have no stage in a tile and run its epilogue all the same."""
+    M, N, bs = 1000, 5000, 128
+    # Block scales up to 200 (e4m3 * b_scale beyond the FP16 range) with small
+    # activations, so that the outputs stay finite.
+    p = wl.make_fp8(M, N, K, bs, dtype, seed=5, bias_sigma=0.05, scale_lo=1.0, scale_hi=200.0,
+                    a_sigma=1e-3)
+    Yr, S = oracle.fp8_matmul(p.A, p.B, p.b_scale, p.bias, M, N, K, bs, p.dtype)
+    assert_within_tolerance(run_fp8(p), Yr, S, dtype, "persistent fp8")
+
+
+def test_one_hot_probe_persistent():
+    """Bit-exact one-hot probe through the persistent kernel: 160 tiles of 256
+    tokens, token m selects column k(m); every CTA's second tile included."""
+    M, N, K, bs = 1024, 5120, 320, 16
+    p = wl.make_fp4(M, N, K, bs, oracle.BF16, seed=23, ws2=1.0)
+    d = fp4_dev(p)
+    W = oracle.fp4_dequantize_f64(p.B_packed, p.weight_scale, 1.0, N, K, bs)
+    ks = (np.arange(M) * 13 + 5) % K
+    A = np.zeros((M, K))
+    A[np.arange(M), ks] = 1.0
+    d["A"] = act_to_dev(wl.act_bits(A, p.dtype), p.dtype)
+    Y = f64_of(run_fp4(p, d))
+    assert np.array_equal(Y, W[:, ks].T)

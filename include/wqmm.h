@@ -28,7 +28,11 @@
  *  - K == 0 with a non-empty output writes Y = bias (or zeros).
  *  - No entry point traps or aborts.  Waits inside the kernels are bounded;
  *    a wait that runs out records WQMM_ERR_TIMEOUT in a device word that
- *    wqmm_device_status() reports, and that call leaves Y untouched.
+ *    wqmm_device_status() reports.  That call then leaves Y untouched,
+ *    except on the persistent paths (the prefill GEMM over enough 256-token
+ *    tiles to fill the GPU, and fp4_fp4_matmul), which store each output
+ *    tile as soon as it is complete: there the tiles finished before the
+ *    wait ran out hold their results and the rest of Y is left untouched.
  *  - Weights are parameters.  The NVFP4 decode GEMV starts copying B_packed
  *    and weight_scale into shared memory before the kernel launched just
  *    before it on `stream` has finished (programmatic dependent launch), so

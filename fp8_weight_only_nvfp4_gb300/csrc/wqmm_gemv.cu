@@ -320,9 +320,11 @@ int launch_general_t(const GemvArgs& a, cudaStream_t st) {
 // * Decode per packed byte: cvt.rn.f16x2.e2m1x2, then for FP16 activations one
 //   f16x2 multiply by the block scale (exact), for BF16 two mixed
 //   f16 x f16 -> f32 multiplies (exact) and one pack to bf16x2 (exact).
-// * Programmatic dependent launch: before griddepcontrol.wait the kernel only
-//   prefetches its weight rows into L2 (never stale: L2 is the point of
-//   coherence), so it may overlap the previous kernel's tail.
+// * Programmatic dependent launch: before griddepcontrol.wait the kernel
+//   prefetches its weight rows into L2 and loads its first chunk of weight
+//   codes and block scales into registers (weights are parameters, not
+//   written by the kernel launched just before), so it overlaps the previous
+//   kernel's tail; the activation is read after the wait.
 // ===========================================================================
 
 constexpr int kFastWarps = 8;
@@ -577,10 +579,11 @@ __global__ void __launch_bounds__(kFastWarps * 32, 2) gemv_fast(const FastParams
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.B + row1 * pitch + off),
                    "r"(wbytes) : "memory");
   }
-  pdl_wait();
-
+  // The first chunk of weight codes and block scales (parameters) before the
+  // dependency wait: 2-4 % per layer in the FP8 chain.
   Chunk<DT, KIND> c0, c1;
   chunk_load<DT, KIND>(c0, p, row0, row1, win_lo, win_hi, t);
+  pdl_wait();
 
   // Stage A[:, win_lo*128 .. win_hi*128) in shared memory (zero beyond K).
   {

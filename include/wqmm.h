@@ -33,12 +33,12 @@
  *    tiles to fill the GPU, and fp4_fp4_matmul), which store each output
  *    tile as soon as it is complete: there the tiles finished before the
  *    wait ran out hold their results and the rest of Y is left untouched.
- *  - Weights are parameters.  The NVFP4 decode GEMV starts copying B_packed
- *    and weight_scale into shared memory, and reads weight_scale_2, before
- *    the kernel launched just before it on `stream` has finished
- *    (programmatic dependent launch), so those three must not be written by
- *    that immediately preceding kernel.  Every other input (A, b_scale,
- *    bias, a_scale) is read only after all earlier work on the stream has
+ *  - Weights are parameters.  The decode GEMVs (M <= 32) start reading the
+ *    weight -- B_packed / B, weight_scale / b_scale and weight_scale_2 --
+ *    before the kernel launched just before them on `stream` has finished
+ *    (programmatic dependent launch), so the weight must not be written by
+ *    that immediately preceding kernel.  Every other input (A, bias,
+ *    a_scale) is read only after all earlier work on the stream has
  *    completed; a bias may be the previous call's output.
  *  - Thread safety: calls may be issued from several host threads at once.
  *    Per-device setup (kernel attributes, driver entry points) runs once.

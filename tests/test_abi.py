@@ -197,3 +197,22 @@ def test_fp4_fp4_matmul_host_checks(L):
     assert f(bias=FAKE_ODD) == 3
     assert f(M=0, A=None, Y=None) == 0
     assert f(N=0, B=None, Y=None) == 0
+
+
+def test_plain_c_caller(L, tmp_path):
+    """The header and library used from C (gcc, no Python in the call path)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    exe = tmp_path / "abi_host_checks"
+    lib_dir = os.path.dirname(wq.library_path())
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c", "abi_host_checks.c"), "-L", lib_dir,
+                        "-lwqmm", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip() == "ok"

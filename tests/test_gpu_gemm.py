@@ -295,3 +295,29 @@ def test_one_hot_probe_persistent():
     d["A"] = act_to_dev(wl.act_bits(A, p.dtype), p.dtype)
     Y = f64_of(run_fp4(p, d))
     assert np.array_equal(Y, W[:, ks].T)
+
+
+def test_persistent_gemm_in_cuda_graph():
+    """The persistent prefill GEMM captured in a CUDA graph: replays equal the
+    eager result bit for bit (no host-side state between calls)."""
+    import torch
+    p = wl.make_fp4(1000, 5000, 640, 16, oracle.BF16, seed=31, bias_sigma=0.05)
+    d = fp4_dev(p)
+    import fp8_weight_only_nvfp4_gb300 as wq
+    eager = run_fp4(p, d)
+    Y = torch.empty_like(eager)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        wq.fp4_weight_matmul(d["A"], d["B"], d["ws"], d["ws2"], d["bias"], 16, out=Y,
+                             stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            wq.fp4_weight_matmul(d["A"], d["B"], d["ws"], d["ws2"], d["bias"], 16, out=Y,
+                                 stream=stream)
+    for _ in range(2):
+        Y.fill_(float("nan"))
+        g.replay()
+        stream.synchronize()
+        assert wq.device_status() == 0
+        assert torch.equal(Y.view(torch.int16), eager.view(torch.int16))

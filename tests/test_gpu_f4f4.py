@@ -243,3 +243,20 @@ def test_f4f4_in_cuda_graph():
         stream.synchronize()
         assert wq.device_status() == 0
         assert torch.equal(Y.view(torch.int16), eager.view(torch.int16))
+
+
+def test_f4f4_full_size_sampled_fp16():
+    """FP4 x FP4 at M = 8192, N = 17408, K = 5120 with FP16 output and bias,
+    random codes and log-uniform scales of both operands: 4096 sampled outputs
+    against the oracle's sum."""
+    M, N, K = 8192, 17408, 5120
+    w = wl.make_fp4(1, N, K, 16, oracle.FP16, seed=8, bias_sigma=0.02)
+    Ac, As = _activation(M, K, oracle.FP16, seed=9, log_uniform=True)
+    Y = f64_of(_run(Ac, As, w, M)).reshape(M, N)
+    Ad = oracle.fp4_dequantize(Ac, As, 1.0, M, K, 16, oracle.FP16)
+    r = np.random.Generator(np.random.PCG64(10))
+    ms = r.integers(0, M, 4096).astype(np.int64)
+    ns = r.integers(0, N, 4096).astype(np.int64)
+    Yr, S = oracle.fp4_matmul_sampled(Ad, w.B_packed, w.weight_scale, w.weight_scale_2, w.bias,
+                                      K, 16, oracle.FP16, ms, ns)
+    assert_within_tolerance(Y[ms, ns], Yr, S, oracle.FP16, "f4f4 full size fp16")

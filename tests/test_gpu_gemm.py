@@ -321,3 +321,27 @@ def test_persistent_gemm_in_cuda_graph():
         stream.synchronize()
         assert wq.device_status() == 0
         assert torch.equal(Y.view(torch.int16), eager.view(torch.int16))
+
+
+@pytest.mark.parametrize("shape", ["gate_up", "down"])
+def test_prefill_full_size_sampled_fp16(shape):
+    """The NVFP4 prefill shapes at M = 8192 with FP16 activations and bias
+    (persistent kernel, FP16 operands): 4096 random outputs plus 4 full rows
+    and 4 full columns against the oracle."""
+    N, K = (17408, 5120) if shape == "gate_up" else (5120, 17408)
+    p = wl.make_fp4(8192, N, K, 16, oracle.FP16, seed=3, ws2=0.0125, bias_sigma=0.02)
+    _sampled_check(p, run_fp4, _fp4_sampled, seed=5)
+
+
+def test_fp8_prefill_sampled_fp16():
+    """FP8 M = 8192, N = 17408, K = 5120, bs = 128 with FP16 activations and
+    block scales up to 200 (each weight row's scales divided by a power of two
+    in the decode and multiplied back in the epilogue), small activations so
+    that the outputs stay finite."""
+    p = wl.make_fp8(8192, 17408, 5120, 128, oracle.FP16, seed=4, scale_lo=0.5, scale_hi=200.0,
+                    bias_sigma=0.02, a_sigma=1e-3)
+
+    def ref(p, ms, ns):
+        return oracle.fp8_matmul_sampled(p.A, p.B, p.b_scale, p.bias, p.K, p.block_size,
+                                         p.dtype, ms, ns)
+    _sampled_check(p, run_fp8, ref, seed=6)

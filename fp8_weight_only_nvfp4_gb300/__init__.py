@@ -395,7 +395,7 @@ def fp4_fp4_matmul(A_packed, A_scale, B_packed, weight_scale, weight_scale_2, bi
     """FP4 x FP4 product on the block-scaled tensor core (FP4 page §6, steps
     2-3): A_packed / A_scale as returned by fp4_quantize_activation, the
     NVFP4 weight with 16-element blocks.  The output type is out.dtype, else
-    bias.dtype, else `dtype` (default bfloat16).  K must be a multiple of 256."""
+    bias.dtype, else `dtype` (default bfloat16).  K must be a multiple of 32."""
     torch = _torch()
     dev = _device_of(A_packed)
     if B_packed.dim() != 2:

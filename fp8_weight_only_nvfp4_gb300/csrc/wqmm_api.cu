@@ -348,9 +348,9 @@ int fp4_fp4_matmul(const uint8_t* A_packed, const uint8_t* A_scale, const uint8_
   if (!Y) return WQMM_ERR_INVALID_ARG;
   if (K > 0 && (!A_packed || !A_scale || !B_packed || !weight_scale || !weight_scale_2))
     return WQMM_ERR_INVALID_ARG;
-  // Stages of 256 k, and scale rows (K / 16 bytes) that the tensor copies can
-  // address: K a multiple of 256.
-  if (K % 256 != 0) return WQMM_ERR_UNSUPPORTED;
+  // Packed code rows (K / 2 bytes) that the tensor copies can address: K a
+  // multiple of 32.
+  if (K % 32 != 0) return WQMM_ERR_UNSUPPORTED;
   if (!aligned16(Y) || (K > 0 && (!aligned16(A_packed) || !aligned16(A_scale) ||
                                   !aligned16(B_packed) || !aligned16(weight_scale) ||
                                   !aligned_n(weight_scale_2, 4))) ||

@@ -132,10 +132,13 @@ __device__ __forceinline__ void mma_f4_stage(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
-template <int DT>
+// GSC: scales from global memory (K % 256 != 0), a separate instantiation so
+// that the tensor-copy path keeps its code unchanged.
+template <int DT, bool GSC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f4f4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmAS, const __grid_constant__ CUtensorMap tmWS,
+                     const uint8_t* __restrict__ as_g, const uint8_t* __restrict__ ws_g,
                      const float* __restrict__ gscale, const uint16_t* __restrict__ bias,
                      uint16_t* __restrict__ Y, int M, int N, int K, int tiles_n, int tiles,
                      int* err) {
@@ -152,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_k = K / kBK;
+  const int num_k = (K + kBK - 1) / kBK;  // a partial last stage reads zero codes past K
+  const int S = K / 16;                      // scale columns (K % 32 == 0)
   // This CTA's tiles: blockIdx.x + i * gridDim.x for i < my_tiles.
   const int my_tiles = (int)blockIdx.x < tiles
                            ? (tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
@@ -175,8 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmW);
-    prefetch_tmap(&tmAS);
-    prefetch_tmap(&tmWS);
+    if constexpr (!GSC) {
+      prefetch_tmap(&tmAS);
+      prefetch_tmap(&tmWS);
+    }
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -197,11 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          mbar_arrive_expect_tx(&full[s], GSC ? (uint32_t)(kActTile + kWTile) : kStageBytes);
           tma_load_2d(smem + kOffAct + s * kActTile, &tmA, k * kRowBytes, m0, &full[s]);
           tma_load_2d(smem + kOffW + s * kWTile, &tmW, k * kRowBytes, n0, &full[s]);
-          tma_load_2d(smem + kOffActSc + s * kActSc, &tmAS, k * kScBytes, m0, &full[s]);
-          tma_load_2d(smem + kOffWSc + s * kWSc, &tmWS, k * kScBytes, n0, &full[s]);
+          if constexpr (!GSC) {
+            tma_load_2d(smem + kOffActSc + s * kActSc, &tmAS, k * kScBytes, m0, &full[s]);
+            tma_load_2d(smem + kOffWSc + s * kWSc, &tmWS, k * kScBytes, n0, &full[s]);
+          }
         }
       }
       // No copy may still be landing in shared memory when the CTA exits.
@@ -258,10 +266,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // columns per chunk, row group (j % 8) of 32 tokens.
       const uint8_t* wsc = smem + kOffWSc + s * kWSc;
       const uint8_t* asc = smem + kOffActSc + s * kActSc;
+      // With K not a multiple of 256 the scale rows cannot be tensor-copied
+      // (row pitch K/16 bytes): this stage's 16 scale bytes of each row come
+      // straight from global memory, zero past the last row or column.
+      const int gi = g / num_k, gk = g - gi * num_k;
+      auto scales16 = [&](const uint8_t* base, int row, int rows) -> uint4 {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (row < rows) {
+          const int64_t off = (int64_t)row * S + 16 * gk;
+          if ((S & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (16 * gk + 4 * j < S) w[j] = __ldg(reinterpret_cast<const uint32_t*>(base + off) + j);
+          } else {
+#pragma unroll
+            for (int b = 0; b < 16; ++b)
+              if (16 * gk + b < S) w[b >> 2] |= (uint32_t)__ldg(base + off + b) << (8 * (b & 3));
+          }
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+      };
       uint32_t va[16], vb[32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint4 r = *reinterpret_cast<const uint4*>(wsc + (32 * c + lane) * kScBytes);
+        uint4 r;
+        if constexpr (GSC)
+          r = scales16(ws_g, tile_n0(gi) + 32 * c + lane, N);
+        else
+          r = *reinterpret_cast<const uint4*>(wsc + (32 * c + lane) * kScBytes);
         va[c] = r.x;
         va[4 + c] = r.y;
         va[8 + c] = r.z;
@@ -269,7 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 r = *reinterpret_cast<const uint4*>(asc + (32 * c + lane) * kScBytes);
+        uint4 r;
+        if constexpr (GSC)
+          r = scales16(as_g, tile_m0(gi) + 32 * c + lane, M);
+        else
+          r = *reinterpret_cast<const uint4*>(asc + (32 * c + lane) * kScBytes);
         vb[c] = r.x;
         vb[8 + c] = r.y;
         vb[16 + c] = r.z;
@@ -343,9 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DT>
+template <int DT, bool GSC>
 int launch_t(const F4F4Args& a, cudaStream_t st) {
   const uint64_t rowb = (uint64_t)a.K / 2, scb = (uint64_t)a.K / 16;
+  constexpr bool gsc = GSC;  // scale rows not tensor-copyable: read them from global memory
   CUtensorMap tmA, tmW, tmAS, tmWS;
   if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, rowb, (uint64_t)a.M, rowb,
                       kRowBytes, kBN, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -353,24 +390,30 @@ int launch_t(const F4F4Args& a, cudaStream_t st) {
       !encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, rowb, (uint64_t)a.N, rowb,
                       kRowBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_tmap_2d(&tmAS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A_scale, scb, (uint64_t)a.M, scb,
-                      kScBytes, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
-      !encode_tmap_2d(&tmWS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ws, scb, (uint64_t)a.N, scb,
-                      kScBytes, kBM, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+      (!gsc && (!encode_tmap_2d(&tmAS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A_scale, scb,
+                                (uint64_t)a.M, scb, kScBytes, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+                !encode_tmap_2d(&tmWS, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ws, scb, (uint64_t)a.N,
+                                scb, kScBytes, kBM, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE))))
     return kCuda;
+  if (gsc) {  // unused by the kernel
+    tmAS = tmA;
+    tmWS = tmW;
+  }
   static std::once_flag once[64];
   const int dev = device_info().device;
   if (dev < 0 || dev >= 64) return kCuda;
   std::call_once(once[dev], [] {
-    cudaFuncSetAttribute(gemm_f4f4_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(gemm_f4f4_kernel<DT, GSC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          kSmemBytes);
   });
   const int64_t tiles_n = (a.N + kBM - 1) / kBM;
   const int64_t tiles = tiles_n * ((a.M + kBN - 1) / kBN);
   const int grid = (int)std::min<int64_t>(tiles, device_info().sm_count);
-  gemm_f4f4_kernel<DT><<<grid, kThreads, kSmemBytes, st>>>(
-      tmA, tmW, tmAS, tmWS, a.gscale, reinterpret_cast<const uint16_t*>(a.bias),
+  gemm_f4f4_kernel<DT, GSC><<<grid, kThreads, kSmemBytes, st>>>(
+      tmA, tmW, tmAS, tmWS, a.A_scale, a.ws, a.gscale,
+      reinterpret_cast<const uint16_t*>(a.bias),
       reinterpret_cast<uint16_t*>(a.Y), (int)a.M, (int)a.N, (int)a.K, (int)tiles_n, (int)tiles,
       device_error_word());
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
@@ -381,7 +424,7 @@ int launch_t(const F4F4Args& a, cudaStream_t st) {
 bool gemm_f4f4_supports(const F4F4Args& a) {
   const DeviceInfo& d = device_info();
   if (d.cc_major != 10 || d.max_smem_optin < kSmemBytes) return false;
-  if (a.K % kBK != 0) return false;
+  if (a.K % 32 != 0) return false;   // packed code rows of 16-byte multiples
   // Tile indices are int.
   const int64_t tiles = ((a.N + kBM - 1) / kBM) * ((a.M + kBN - 1) / kBN);
   return tiles < (int64_t(1) << 31) && a.N < (int64_t(1) << 31);
@@ -389,7 +432,8 @@ bool gemm_f4f4_supports(const F4F4Args& a) {
 
 int launch_gemm_f4f4(const F4F4Args& a, cudaStream_t st) {
   if (!gemm_f4f4_supports(a)) return kUnsupported;
-  return a.dtype == 1 ? launch_t<1>(a, st) : launch_t<0>(a, st);
+  if (a.K % kBK != 0) return a.dtype == 1 ? launch_t<1, true>(a, st) : launch_t<0, true>(a, st);
+  return a.dtype == 1 ? launch_t<1, false>(a, st) : launch_t<0, false>(a, st);
 }
 
 }  // namespace wqmm

@@ -104,7 +104,7 @@ struct F4F4Args {
   int dtype;
 };
 // Returns kUnsupported if the device or the shape cannot take this path
-// (K % 256 != 0).
+// (K % 32 != 0).
 int launch_gemm_f4f4(const F4F4Args& a, cudaStream_t st);
 bool gemm_f4f4_supports(const F4F4Args& a);
 

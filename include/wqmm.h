@@ -283,8 +283,9 @@ int fp4_quantize_dequantize_activation(const void* A, void* out, int64_t M, int6
  *   Y             [M, N] dtype (dtype selects only the output and bias type).
  * Block scales are read as unsigned E4M3 (the tensor core's scale type): the
  * sign bit must be clear and 0x7F (NaN) is not allowed; the quantizer's
- * scales always qualify.  K must be a multiple of 256 (WQMM_ERR_UNSUPPORTED
- * otherwise); K == 0 writes Y = bias (or 0).
+ * scales always qualify.  K must be a multiple of 32 (WQMM_ERR_UNSUPPORTED
+ * otherwise; a multiple of 256 takes the fastest path); K == 0 writes
+ * Y = bias (or 0).
  * Errors: odd K, a size < 0 or a NULL pointer -> INVALID_ARG; a pointer not
  * 16-byte aligned (weight_scale_2 4, bias 2) -> MISALIGNED.
  * Accuracy: the bound of fp4_weight_matmul with sum_k |A_q * B_dq| in place

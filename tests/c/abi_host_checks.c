@@ -43,7 +43,7 @@ int main(void) {
                                         (int64_t)(WQMM_NOALLOC_SCRATCH_BYTES / (2 * 4096)) + 1, 64,
                                         4096, 128, WQMM_BF16, NULL),
          WQMM_ERR_UNSUPPORTED);
-  expect("fp4 x fp4 K", fp4_fp4_matmul(fake, fake, fake, fake, fake, NULL, fake, 16, 32, 128,
+  expect("fp4 x fp4 K", fp4_fp4_matmul(fake, fake, fake, fake, fake, NULL, fake, 16, 32, 48,
                                        WQMM_BF16, NULL), WQMM_ERR_UNSUPPORTED);
   expect("actq odd K", fp4_quantize_activation(fake, fake, fake, 4, 33, WQMM_BF16, NULL),
          WQMM_ERR_INVALID_ARG);

@@ -186,7 +186,7 @@ def test_fp4_fp4_matmul_host_checks(L):
     assert f(dt=3) == 1
     assert f(K=255) == 1              # odd K
     assert f(M=-1) == 1
-    assert f(K=128) == 2              # K must be a multiple of 256
+    assert f(K=48) == 2               # K must be a multiple of 32
     assert f(K=1 << 31) == 2
     assert f(A=None) == 1
     assert f(As=None) == 1

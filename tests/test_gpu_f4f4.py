@@ -207,13 +207,25 @@ def test_f4f4_k0_and_empty():
 
 
 def test_f4f4_unsupported_k():
-    """K not a multiple of 256 is refused (no launch)."""
-    A = torch.zeros(4, 64, dtype=torch.uint8, device=DEV)
+    """K not a multiple of 32 is refused (no launch)."""
+    A = torch.zeros(4, 40, dtype=torch.uint8, device=DEV)
     with pytest.raises(wq.WqmmError):
-        wq.fp4_fp4_matmul(A, torch.zeros(4, 8, dtype=torch.uint8, device=DEV),
-                          torch.zeros(16, 64, dtype=torch.uint8, device=DEV),
-                          torch.zeros(16, 8, dtype=torch.uint8, device=DEV),
+        wq.fp4_fp4_matmul(A, torch.zeros(4, 5, dtype=torch.uint8, device=DEV),
+                          torch.zeros(16, 40, dtype=torch.uint8, device=DEV),
+                          torch.zeros(16, 5, dtype=torch.uint8, device=DEV),
                           torch.ones(1, device=DEV))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("M,N,K", [(300, 200, 32), (257, 384, 96), (64, 1000, 480),
+                                   (513, 129, 1056), (200, 300, 5152), (9, 100, 5024)])
+def test_f4f4_k_not_multiple_of_256(M, N, K, dtype):
+    """K % 256 != 0: the scale rows are read from global memory (4-byte loads
+    when K % 64 == 0, byte loads otherwise) and the last stage is partial."""
+    w = wl.make_fp4(1, N, K, 16, dtype, seed=M + N + K + 1, bias_sigma=0.1)
+    Ac, As = _activation(M, K, dtype, seed=5 * M + K, log_uniform=(K % 64 != 0))
+    Yr, S = _reference(Ac, As, w, M)
+    assert_within_tolerance(_run(Ac, As, w, M), Yr, S, dtype, f"f4f4 {M}x{N}x{K}")
 
 
 def test_f4f4_in_cuda_graph():

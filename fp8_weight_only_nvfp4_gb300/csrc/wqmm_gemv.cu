@@ -1095,6 +1095,11 @@ static int tma_stage_bytes(int nt) {
 // dependent launch); with many column groups that is one rank per group.
 // The ranks' partial sums must also fit in rank 0's ring.
 // Measured on GB300 for N = K = 5120, M = 4: C = 3 beats 1, 2, 4, 5 and 7.
+// With two activation tiles (9..16 rows) a CTA does twice the MMA work per
+// step and three of them are resident per SM: up to three per SM (C = 5)
+// took 9.5 instead of 11.8 us per layer in the chain; with three or four
+// tiles only two are resident, and the same rule ran in two waves (15.9 /
+// 18.6 instead of 11.4 / 13.3 us).
 bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
   if (a.kind != 0 || a.bs != 16 || a.K % 256 != 0 || a.M < 1 || a.M > kTMaxM) return false;
   if (a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 30)) return false;
@@ -1108,7 +1113,7 @@ bool plan_tma(const GemvArgs& a, TmaPlan& pl) {
     const int spc = (nsteps + c - 1) / c;
     if (spc < 2) break;
     const int ce = (nsteps + spc - 1) / spc;
-    if (groups * ce > 2 * (int64_t)d.sm_count) break;
+    if (groups * ce > (nt == 2 ? 3 : 2) * (int64_t)d.sm_count) break;
     if (ce * kTCons * nt * 512 > std::min(spc, 4) * stage) break;
     C = ce;
   }

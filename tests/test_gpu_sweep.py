@@ -5,8 +5,9 @@ Each case draws its shape inside a family chosen to land on one path -- the
 TMA decode GEMV (up to 32 rows), the register-fed and the general GEMV, the
 narrow-tile GEMM (light CTAs or a cluster K split), the persistent 256-token
 GEMM, the FP8 paths, the W8A8 workspace path and the FP4 x FP4 GEMM -- with
-ragged sizes, block sizes, both activation types and optional bias.  The
-shapes are fixed by the seed, so a failure reproduces."""
+ragged sizes, block sizes, both activation types and optional bias.  Seven
+seeds draw 33 shapes each; the shapes are fixed by the seed, so a failure
+reproduces (the seed is part of the test id)."""
 
 import numpy as np
 import pytest
@@ -27,7 +28,7 @@ def _families(seed=2024):
 
     def add(kind, M, N, K, bs):
         cases.append((kind, int(M), int(N), int(K), int(bs), int(r.integers(0, 2)),
-                      bool(r.integers(0, 2)), int(r.integers(0, 1 << 20))))
+                      bool(r.integers(0, 2)), int(r.integers(0, 1 << 20)), seed))
     for _ in range(5):   # TMA decode GEMV: M <= 32, bs 16, K % 256 == 0
         add("fp4", r.integers(1, 33), r.integers(1, 700), 256 * r.integers(1, 9), 16)
     for _ in range(4):   # register-fed GEMV: other power-of-two blocks
@@ -52,17 +53,19 @@ def _families(seed=2024):
     return cases
 
 
-CASES = _families()
+SEEDS = range(2024, 2031)
+CASES = [c for s in SEEDS for c in _families(s)]
 
 
 def _id(c):
-    kind, M, N, K, bs, dt, bias, seed = c
-    return f"{kind}-M{M}-N{N}-K{K}-bs{bs}-{'bf16' if dt else 'fp16'}{'-bias' if bias else ''}"
+    kind, M, N, K, bs, dt, bias, seed, family_seed = c
+    return (f"s{family_seed}-{kind}-M{M}-N{N}-K{K}-bs{bs}-{'bf16' if dt else 'fp16'}"
+            f"{'-bias' if bias else ''}")
 
 
 @pytest.mark.parametrize("case", CASES, ids=[_id(c) for c in CASES])
 def test_sweep(case):
-    kind, M, N, K, bs, dt, bias, seed = case
+    kind, M, N, K, bs, dt, bias, seed, _ = case
     dtype = oracle.BF16 if dt else oracle.FP16
     sigma = 0.05 if bias else None
     if kind == "fp4":

@@ -29,3 +29,15 @@ def test_dequant_and_actq_bytes():
 
 def test_prefill_flops():
     assert 2 * 8192 * 17408 * 5120 == 1_460_288_880_640
+
+
+def test_recorded_traffic_matches_current_sources():
+    """The DRAM bytes the bench line reports for the headline kernel come from
+    a committed ncu record keyed by a hash of that kernel's sources; the
+    record must have been taken on the sources as they stand (a kernel change
+    needs a new capture), and it must equal the algorithmic bytes within 1 %
+    (no re-reads) for the figure to mean what the line says."""
+    t = bench.recorded_traffic("gemv_decode_M4_N5120_K5120")
+    assert t is not None, "profiles/ncu_traffic.json predates the current GEMV sources"
+    alg = bench.gemv_bytes(4, 5120, 5120)
+    assert abs(t - alg) / alg < 0.01

@@ -72,7 +72,10 @@ constexpr int kAccCol = 0;     // accumulator: columns [0, BN)
 //           each, for the narrow token tiles: there the pace of one CTA's
 //           stage loop, not the SM's MMA or decode throughput, bounds the
 //           time, and a second resident CTA (with a K split) runs another
-//           stage loop beside it.
+//           stage loop beside it.  Four quarter-size CTAs per SM (one decoder
+//           warp per lane quarter, 128 columns) were measured no faster than
+//           two: from the second one on, the CTAs' common share of the SM
+//           sets the pace.
 template <int PH>
 struct Shape {
   static constexpr int ctas_per_sm = PH == 2 ? 2 : 1;

@@ -649,12 +649,15 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(config(1), workload="NVFP4 decode GEMV M=4 N=5120 K=5120 bs=16 BF16, "
-                                           "one layer per step (CPU oracle)",
-                       l2="not applicable (host cores)"),
+        # The same workload as the CUDA arm's line; each step is a bounded
+        # sample of it (one of its layers, M = 4, N = K = 5120), and the value
+        # counts the bytes of the layers actually processed.
+        "config": config(),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle",
-                         "sample": f"{args.steps} timed full oracle calls of one layer"},
+                         "sample": f"each step one layer of the {LAYERS}-layer chain (M=4, "
+                                   f"N=K=5120, NVFP4, float64, {threads} threads); "
+                                   f"{args.steps} timed steps"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

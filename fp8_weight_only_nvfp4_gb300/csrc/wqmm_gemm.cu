@@ -623,7 +623,8 @@ __global__ void __launch_bounds__(Shape<PH>::threads, Shape<PH>::ctas_per_sm)
 
 // Persistent form of gemm_tc_kernel for the 256-token prefill tile without a
 // K split: one CTA per SM walks the tiles blockIdx.x, blockIdx.x + gridDim.x,
-// ... (weight-row tiles fastest).  Producer, decoders and MMA run on across
+// ... (NVFP4: weight-row tiles fastest; FP8: bands of token tiles, see the
+// walk below).  Producer, decoders and MMA run on across
 // tile boundaries -- the producer keeps filling the ring with the next tile's
 // stages while the current one finishes -- and the decoders run each tile's
 // epilogue as soon as their own last stage of it is done: they read their
